@@ -1,0 +1,187 @@
+/*
+ * Sequential fp64 oracle for the Mamba selective state-space scan and its
+ * single-token decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct CPU
+ * statement of what the GPU path computes. Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg may load it. It shares no code,
+ * header, table or helper with the CUDA library, and the CUDA library never
+ * calls it.
+ *
+ * What it follows (page titles and the passage on each page):
+ *   [SSM]  "State Space Models and Mamba" (jonathanding.github.io, llm-learning)
+ *          §1  continuous system x' = A x + B u, y = C x + D u
+ *          §1.5 S4D-Real: A stored as A_log, A = -exp(A_log)
+ *          §2  zero-order-hold discretisation: Abar = exp(dt A),
+ *              Bbar = A^-1 (exp(dt A) - I) B; recurrence x_k = Abar x_{k-1} + Bbar u_k
+ *          §4  selectivity: dt_k = softplus(Linear(u_k)), B_k, C_k per step
+ *   [NOTES] "Mamba" paper notes (awesome.papernotes.org, 2023_mamba)
+ *          "Design 1: Selective State Space": Bbar = (dt A)^-1 (exp(dt A) - I) dt B,
+ *          and the selective_ssm sketch: y + D * x skip
+ *          "Overall framework": out = y * SiLU(z)
+ *   [COMP] "Mamba" concept page (compassingai.com) §3.1: the same discrete update
+ *
+ * Because A is diagonal, (dt A)^-1 (exp(dt A) - I) dt B is elementwise per
+ * state n: Bbar_n = expm1(dt A_n) / (dt A_n) * dt * B_n. This file writes it in
+ * exactly that form, with the limit expm1(x)/x -> 1 taken when dt A_n == 0.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - the scan starts from h = 0 unless an initial state is passed;
+ *   - delta_bias is added before softplus; a NULL bias, D or z means 0 / 0 / no gate;
+ *   - the gate multiplies after the D skip: out = (C.h + D u) * z * sigmoid(z);
+ *   - softplus is exact: max(x,0) + log1p(exp(-|x|)), no cut-off.
+ *
+ * Layouts (row-major, contiguous):
+ *   u, delta, z, out : (batch, seqlen, dim)
+ *   B, C             : (batch, seqlen, dstate)
+ *   A_log            : (dim, dstate)
+ *   D, delta_bias    : (dim)
+ *   h0, last_state   : (batch, dim, dstate)
+ *   decode: u, delta, z, out : (batch, dim); B, C : (batch, dstate);
+ *           state : (batch, dim, dstate), updated in place.
+ *
+ * The variant flag selects the input matrix: 0 = zero-order hold (the method),
+ * 1 = the simplified Bbar = dt * B that the paper-notes sketch and the
+ * first-order (Euler) reading of [SSM] §2 give. Variant 1 is kept for the
+ * optional simplified-discretisation row only.
+ */
+#include <math.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#else
+static int omp_get_max_threads(void) { return 1; }
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARG 1
+/* Largest state size the oracle accepts (per-channel scratch lives on the stack). */
+#define ORACLE_MAX_DSTATE 1024
+
+/* [SSM] §4: dt = softplus(.), written as the overflow-free identity
+ * log(1 + e^x) = max(x, 0) + log1p(e^-|x|). */
+static double oracle_softplus(double x)
+{
+    return fmax(x, 0.0) + log1p(exp(-fabs(x)));
+}
+
+/* [NOTES] "Overall framework": SiLU(z) = z * sigmoid(z). */
+static double oracle_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/* Zero-order-hold input coefficient for one state, [NOTES] Design 1 /
+ * [SSM] §2: (dt A)^-1 (exp(dt A) - 1) dt B, elementwise because A is
+ * diagonal. */
+static double oracle_bbar(double dt, double A_n, double B_n, int variant)
+{
+    if (variant == 1)
+        return dt * B_n;
+    double dA = dt * A_n;
+    double phi = (dA == 0.0) ? 1.0 : expm1(dA) / dA;
+    return phi * dt * B_n;
+}
+
+/* One channel (b, d) of the scan, sequential over t. */
+static void oracle_scan_channel(long b, long d, long dim, long dstate, long seqlen,
+                                const double *u, const double *delta,
+                                const double *A_log, const double *B,
+                                const double *C, const double *D,
+                                const double *z, const double *delta_bias,
+                                const double *h0, double *out,
+                                double *last_state, int variant, double *h,
+                                double *A)
+{
+    for (long n = 0; n < dstate; ++n) {
+        A[n] = -exp(A_log[d * dstate + n]); /* [SSM] §1.5 */
+        h[n] = h0 ? h0[(b * dim + d) * dstate + n] : 0.0;
+    }
+    const double bias = delta_bias ? delta_bias[d] : 0.0;
+    for (long t = 0; t < seqlen; ++t) {
+        const long i = (b * seqlen + t) * dim + d;   /* (b, t, d) */
+        const long j = (b * seqlen + t) * dstate;    /* (b, t, 0) */
+        const double dt = oracle_softplus(delta[i] + bias);
+        double y = 0.0;
+        for (long n = 0; n < dstate; ++n) {
+            const double abar = exp(dt * A[n]);                       /* [SSM] §2 */
+            const double bbar = oracle_bbar(dt, A[n], B[j + n], variant);
+            h[n] = abar * h[n] + bbar * u[i];                         /* recurrence */
+            y += C[j + n] * h[n];                                     /* y = C h */
+        }
+        if (D)
+            y += D[d] * u[i];                                         /* D skip */
+        if (z)
+            y *= oracle_silu(z[i]);                                   /* gate */
+        out[i] = y;
+    }
+    if (last_state)
+        for (long n = 0; n < dstate; ++n)
+            last_state[(b * dim + d) * dstate + n] = h[n];
+}
+
+/* Whole scan. nthreads <= 0 uses the OpenMP default; channels are
+ * independent, so the parallel loop changes no arithmetic. */
+int oracle_selective_scan(long batch, long dim, long dstate, long seqlen,
+                          const double *u, const double *delta,
+                          const double *A_log, const double *B, const double *C,
+                          const double *D, const double *z,
+                          const double *delta_bias, const double *h0,
+                          double *out, double *last_state, int variant,
+                          int nthreads)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0 || seqlen < 0)
+        return ORACLE_BAD_ARG;
+    if (batch == 0 || dim == 0)
+        return ORACLE_OK;
+    if ((seqlen > 0 && (!u || !delta || !B || !C || !out)) || !A_log)
+        return ORACLE_BAD_ARG;
+    if (dstate > ORACLE_MAX_DSTATE)
+        return ORACLE_BAD_ARG;
+    const long nch = batch * dim;
+#pragma omp parallel for schedule(static) num_threads(nthreads > 0 ? nthreads : omp_get_max_threads())
+    for (long c = 0; c < nch; ++c) {
+        double h[ORACLE_MAX_DSTATE], A[ORACLE_MAX_DSTATE];
+        oracle_scan_channel(c / dim, c % dim, dim, dstate, seqlen, u, delta,
+                            A_log, B, C, D, z, delta_bias, h0, out,
+                            last_state, variant, h, A);
+    }
+    return ORACLE_OK;
+}
+
+/* Single-token decode step on a resident state, [SSM] §3 recurrence mode:
+ * the same body as one step of the scan, starting from the given state. */
+int oracle_state_update(long batch, long dim, long dstate, double *state,
+                        const double *u, const double *delta,
+                        const double *A_log, const double *B, const double *C,
+                        const double *D, const double *z,
+                        const double *delta_bias, double *out, int variant)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0)
+        return ORACLE_BAD_ARG;
+    if (batch == 0 || dim == 0)
+        return ORACLE_OK;
+    if (!state || !u || !delta || !A_log || !B || !C || !out || dstate > ORACLE_MAX_DSTATE)
+        return ORACLE_BAD_ARG;
+    for (long b = 0; b < batch; ++b) {
+        for (long d = 0; d < dim; ++d) {
+            const long i = b * dim + d;
+            const double dt = oracle_softplus(delta[i] + (delta_bias ? delta_bias[d] : 0.0));
+            double y = 0.0;
+            for (long n = 0; n < dstate; ++n) {
+                const double A_n = -exp(A_log[d * dstate + n]);
+                const double abar = exp(dt * A_n);
+                const double bbar = oracle_bbar(dt, A_n, B[b * dstate + n], variant);
+                double *h = &state[i * dstate + n];
+                *h = abar * (*h) + bbar * u[i];
+                y += C[b * dstate + n] * (*h);
+            }
+            if (D)
+                y += D[d] * u[i];
+            if (z)
+                y *= oracle_silu(z[i]);
+            out[i] = y;
+        }
+    }
+    return ORACLE_OK;
+}

@@ -1,0 +1,345 @@
+"""Checks that tie the fp64 oracle to facts fixed by the pages and by mathematics.
+
+Each ``pin_*`` function runs one oracle (an ``oracle.OracleLib``) on a small
+case and returns the worst error it saw against a reference that does NOT reuse
+the oracle's formulas: an ODE integrated with Runge-Kutta, a quadrature of the
+zero-order-hold integral, a closed form, or a brute-force product-sum. The
+thresholds live with each pin in ``PINS`` so that the planted-mistake test can
+run the same checks against deliberately broken copies of the oracle.
+
+Sources (page titles and passages):
+  "State Space Models and Mamba" (jonathanding.github.io):
+     §2 zero-order hold (the exact solution of x' = A x + B u over one step with
+        u held constant), §3 recurrence/convolution duality y_k = sum_j C Abar^(k-j) Bbar u_j,
+     §4 Theorem 1 (N=1, A=-1, B=1 is the gated RNN h = (1-g) h + g x with
+        g = sigmoid(.)), the large/small dt behaviour ("reset & focus" /
+        "persist & ignore"), the associative operator of the parallel scan,
+     §5 the semiseparable form with products of a_t (the brute force below).
+  "Mamba" paper notes (awesome.papernotes.org): selective_ssm sketch (D skip),
+     overall framework (out = y * SiLU(z)).
+"""
+from __future__ import annotations
+
+import numpy as np
+from scipy import integrate
+from scipy.special import expit
+
+
+# ---------------------------------------------------------------- references
+def softplus_ref(x):
+    # log(1 + e^x) through numpy's logaddexp, not the oracle's log1p form.
+    return np.logaddexp(0.0, x)
+
+
+def silu_ref(z):
+    return z * expit(z)
+
+
+def zoh_integral(A, dt):
+    """int_0^dt exp(A tau) d tau by adaptive quadrature, elementwise."""
+    A = np.asarray(A, np.float64)
+    dt = np.broadcast_to(np.asarray(dt, np.float64), A.shape)
+    out = np.empty(A.shape)
+    for idx in np.ndindex(A.shape):
+        a, T = A[idx], dt[idx]
+        val, _ = integrate.quad(lambda s: np.exp(a * s), 0.0, T, epsabs=0.0, epsrel=1e-13, limit=200)
+        out[idx] = val
+    return out
+
+
+def rk4_linear(h0, A, forcing, T, steps=10000):
+    """Integrate h' = A h + forcing (all elementwise, constant in time) over [0, T]."""
+    h = np.array(h0, np.float64)
+    k = T / steps
+
+    def f(x):
+        return A * x + forcing
+
+    for _ in range(steps):
+        k1 = f(h)
+        k2 = f(h + 0.5 * k * k1)
+        k3 = f(h + 0.5 * k * k2)
+        k4 = f(h + k * k3)
+        h = h + (k / 6.0) * (k1 + 2 * k2 + 2 * k3 + k4)
+    return h
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = max(np.max(np.abs(ref)), 1e-300)
+    return float(np.max(np.abs(got - ref)) / scale)
+
+
+# ---------------------------------------------------------------------- pins
+def pin_zoh_matches_ode(orc, seed=0):
+    """One decode step equals the exact solution of the continuous system over dt."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N = 2, 3, 4
+    A_log = rng.uniform(-1.0, 2.5, (dim, N))
+    state0 = rng.standard_normal((batch, dim, N))
+    u = rng.standard_normal((batch, dim))
+    B = rng.standard_normal((batch, N))
+    C = rng.standard_normal((batch, N))
+    delta = rng.uniform(-4.0, 1.5, (batch, dim))
+    bias = rng.uniform(-0.5, 0.5, dim)
+    new, out = orc.state_update(state0, u, delta, A_log, B, C, delta_bias=bias)
+    dt = softplus_ref(delta + bias)[:, :, None]
+    A = -np.exp(A_log)[None]
+    forcing = B[:, None, :] * u[:, :, None]
+    h_ref = rk4_linear(state0, A, forcing, dt)
+    y_ref = np.einsum("bn,bdn->bd", C, h_ref)
+    return max(rel_err(new, h_ref), rel_err(out, y_ref))
+
+
+def pin_lti_convolution(orc, seed=1):
+    """Constant dt, B, C: the scan equals the convolution with K_i = C Abar^i Bbar."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L = 2, 3, 4, 40
+    A_log = rng.uniform(-0.5, 1.5, (dim, N))
+    c = rng.uniform(-4.0, 0.0, (batch, dim))
+    delta = np.broadcast_to(c[:, None, :], (batch, L, dim)).copy()
+    Bc = rng.standard_normal((batch, N))
+    Cc = rng.standard_normal((batch, N))
+    B = np.broadcast_to(Bc[:, None, :], (batch, L, N)).copy()
+    C = np.broadcast_to(Cc[:, None, :], (batch, L, N)).copy()
+    u = rng.standard_normal((batch, L, dim))
+    D = rng.standard_normal(dim)
+    out, last = orc.selective_scan(u, delta, A_log, B, C, D=D)
+    A = -np.exp(A_log)                                   # (dim, N)
+    dt = softplus_ref(c)                                 # (batch, dim)
+    Abar = np.exp(dt[:, :, None] * A[None])              # (batch, dim, N)
+    Bbar = zoh_integral(np.broadcast_to(A[None], Abar.shape), dt[:, :, None]) * Bc[:, None, :]
+    powers = Abar[..., None] ** np.arange(L)             # (batch, dim, N, L)
+    K = np.einsum("bn,bdni->bdi", Cc, powers * Bbar[..., None])
+    y = np.zeros((batch, L, dim))
+    for k in range(L):
+        y[:, k, :] = np.einsum("bdj,bjd->bd", K[:, :, k::-1], u[:, : k + 1, :]) + D * u[:, k, :]
+    h_last = np.einsum("bdnj,bjd->bdn", powers[..., ::-1] * Bbar[..., None], u)
+    return max(rel_err(out, y), rel_err(last, h_last))
+
+
+def pin_n1_geometric(orc, seed=2):
+    """N=1, constant dt, u=B=C=1: h_k = bbar (1 - a^(k+1)) / (1 - a)."""
+    rng = np.random.default_rng(seed)
+    L = 64
+    A_log = np.array([[rng.uniform(-0.5, 1.0)]])
+    c = rng.uniform(-3.0, 0.5)
+    delta = np.full((1, L, 1), c)
+    ones = np.ones((1, L, 1))
+    out, last = orc.selective_scan(ones, delta, A_log, ones, ones)
+    A = -np.exp(A_log[0, 0])
+    dt = softplus_ref(c)
+    a = np.exp(dt * A)
+    bbar = zoh_integral(np.array([A]), dt)[0]
+    k = np.arange(L)
+    h = bbar * (1.0 - a ** (k + 1)) / (1.0 - a)
+    return max(rel_err(out[0, :, 0], h), rel_err(last[0, 0, 0], h[-1]))
+
+
+def pin_theorem1_gated_rnn(orc, seed=3):
+    """N=1, A=-1, B=C=1: h_t = (1 - g_t) h_{t-1} + g_t x_t with g_t = sigmoid(delta_t + bias)."""
+    rng = np.random.default_rng(seed)
+    batch, dim, L = 2, 3, 50
+    A_log = np.zeros((dim, 1))
+    delta = rng.normal(0.0, 2.0, (batch, L, dim))
+    bias = rng.uniform(-1.0, 1.0, dim)
+    x = rng.standard_normal((batch, L, dim))
+    ones = np.ones((batch, L, 1))
+    out, last = orc.selective_scan(x, delta, A_log, ones, ones, delta_bias=bias)
+    g = expit(delta + bias)
+    h = np.zeros((batch, dim))
+    ref = np.zeros_like(x)
+    for t in range(L):
+        h = (1.0 - g[:, t]) * h + g[:, t] * x[:, t]
+        ref[:, t] = h
+    return max(rel_err(out, ref), rel_err(last[..., 0], h))
+
+
+def pin_small_dt_persists(orc, seed=4):
+    """delta + bias = -40 (dt ~ 4e-18): the state persists and the input is ignored."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L = 2, 3, 4, 10
+    A_log = rng.uniform(-0.5, 2.0, (dim, N))
+    state0 = rng.standard_normal((batch, dim, N))
+    u = rng.standard_normal((batch, dim))
+    B = rng.standard_normal((batch, N))
+    C = rng.standard_normal((batch, N))
+    D = rng.standard_normal(dim)
+    z = rng.standard_normal((batch, dim))
+    delta = np.full((batch, dim), -40.0)
+    new, out = orc.state_update(state0, u, delta, A_log, B, C, D=D, z=z)
+    y_ref = (np.einsum("bn,bdn->bd", C, state0) + D * u) * silu_ref(z)
+    e1 = max(rel_err(new, state0), rel_err(out, y_ref))
+    # scan from zero: the output is the D skip alone
+    us = rng.standard_normal((batch, L, dim))
+    zs = rng.standard_normal((batch, L, dim))
+    Bs = rng.standard_normal((batch, L, N))
+    Cs = rng.standard_normal((batch, L, N))
+    outs, lasts = orc.selective_scan(us, np.full((batch, L, dim), -40.0), A_log, Bs, Cs, D=D, z=zs)
+    e2 = rel_err(outs, D * us * silu_ref(zs))
+    return max(e1, e2, float(np.max(np.abs(lasts))))
+
+
+def pin_large_dt_memoryless(orc, seed=5):
+    """delta + bias = +40: Abar ~ e^-40|A|, so h_t = B_t u_t / |A| and y is memoryless."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L = 2, 3, 4, 12
+    A_log = rng.uniform(0.0, 2.0, (dim, N))
+    u = rng.standard_normal((batch, L, dim))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    D = rng.standard_normal(dim)
+    out, last = orc.selective_scan(u, np.full((batch, L, dim), 40.0), A_log, B, C, D=D)
+    absA = np.exp(A_log)
+    h = B[:, :, None, :] * u[..., None] / absA[None, None]     # (batch, L, dim, N)
+    y = np.einsum("btn,btdn->btd", C, h) + D * u
+    return max(rel_err(out, y), rel_err(last, h[:, -1]))
+
+
+def brute_force_scan(u, delta, A_log, B, C, D=None, z=None, bias=None):
+    """y_t = sum_n C_t[n] sum_{j<=t} (prod_{i=j+1..t} Abar_i[n]) Bbar_j[n] u_j (+ D u_t), gated.
+
+    O(L^2) product-sum with Bbar from quadrature; independent of the recurrence."""
+    batch, L, dim = u.shape
+    N = A_log.shape[1]
+    A = -np.exp(A_log)
+    x = delta + (0.0 if bias is None else bias)
+    dt = softplus_ref(x)                                           # (batch, L, dim)
+    Abar = np.exp(dt[..., None] * A[None, None])                   # (batch, L, dim, N)
+    Bbar = zoh_integral(np.broadcast_to(A[None, None], Abar.shape), dt[..., None]) * B[:, :, None, :]
+    out = np.zeros((batch, L, dim))
+    last = np.zeros((batch, dim, N))
+    for t in range(L):
+        h_t = np.zeros((batch, dim, N))
+        for j in range(t + 1):
+            prod = np.ones((batch, dim, N))
+            for i in range(j + 1, t + 1):
+                prod = prod * Abar[:, i]
+            h_t = h_t + prod * Bbar[:, j] * u[:, j, :, None]
+        y = np.einsum("bn,bdn->bd", C[:, t], h_t)
+        if D is not None:
+            y = y + D * u[:, t]
+        if z is not None:
+            y = y * silu_ref(z[:, t])
+        out[:, t] = y
+        last = h_t
+    return out, last
+
+
+def pin_brute_force(orc, seed=6, cases=6):
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    for _ in range(cases):
+        batch, dim, N, L = (int(rng.integers(1, 3)), int(rng.integers(1, 5)),
+                            int(rng.integers(1, 5)), int(rng.integers(1, 17)))
+        A_log = rng.uniform(-1.0, 2.0, (dim, N))
+        u = rng.standard_normal((batch, L, dim))
+        delta = rng.normal(-1.0, 1.5, (batch, L, dim))
+        B = rng.standard_normal((batch, L, N))
+        C = rng.standard_normal((batch, L, N))
+        D = rng.standard_normal(dim)
+        z = rng.standard_normal((batch, L, dim))
+        bias = rng.uniform(-1.0, 1.0, dim)
+        out, last = orc.selective_scan(u, delta, A_log, B, C, D=D, z=z, delta_bias=bias)
+        ref_out, ref_last = brute_force_scan(u, delta, A_log, B, C, D, z, bias)
+        worst = max(worst, rel_err(out, ref_out), rel_err(last, ref_last))
+    return worst
+
+
+def pin_associative_operator(orc, seed=7):
+    """Composing (a_t, b_t) pairs with (a,b)o(a',b') = (a a', a' b + b') over a random
+    bracketing gives the scan's final state."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L = 1, 2, 3, 23
+    A_log = rng.uniform(-0.5, 2.0, (dim, N))
+    u = rng.standard_normal((batch, L, dim))
+    delta = rng.normal(-1.0, 1.0, (batch, L, dim))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    _, last = orc.selective_scan(u, delta, A_log, B, C)
+    A = -np.exp(A_log)
+    dt = softplus_ref(delta)[0]                                   # (L, dim)
+    a = np.exp(dt[..., None] * A[None])                           # (L, dim, N)
+    b = zoh_integral(np.broadcast_to(A[None], a.shape), dt[..., None]) * B[0][:, None, :] * u[0][..., None]
+    pairs = [(a[t], b[t]) for t in range(L)]
+
+    def combine(left, right):        # left acts first in time
+        return (left[0] * right[0], right[0] * left[1] + right[1])
+
+    while len(pairs) > 1:            # random bracketing
+        k = int(rng.integers(0, len(pairs) - 1))
+        pairs[k:k + 2] = [combine(pairs[k], pairs[k + 1])]
+    return rel_err(last[0], pairs[0][1])
+
+
+def pin_continuation(orc, seed=8):
+    """scan(0..L1) then scan(L1..L) from its last_state, or then decode steps, equals scan(0..L)."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L, L1 = 2, 3, 4, 30, 17
+    A_log = rng.uniform(-0.5, 2.0, (dim, N))
+    u = rng.standard_normal((batch, L, dim))
+    delta = rng.normal(-2.0, 1.0, (batch, L, dim))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    D = rng.standard_normal(dim)
+    z = rng.standard_normal((batch, L, dim))
+    bias = rng.uniform(-1, 1, dim)
+    full, last = orc.selective_scan(u, delta, A_log, B, C, D, z, bias)
+    o1, s1 = orc.selective_scan(u[:, :L1], delta[:, :L1], A_log, B[:, :L1], C[:, :L1], D, z[:, :L1], bias)
+    o2, s2 = orc.selective_scan(u[:, L1:], delta[:, L1:], A_log, B[:, L1:], C[:, L1:], D, z[:, L1:], bias, h0=s1)
+    e = max(rel_err(np.concatenate([o1, o2], 1), full), rel_err(s2, last))
+    state = s1
+    outs = []
+    for t in range(L1, L):
+        state, o = orc.state_update(state, u[:, t], delta[:, t], A_log, B[:, t], C[:, t], D, z[:, t], bias)
+        outs.append(o)
+    e = max(e, rel_err(np.stack(outs, 1), full[:, L1:]), rel_err(state, last))
+    return e
+
+
+def pin_structure(orc, seed=9):
+    """u = 0 gives 0; causality; linearity in u; z = 0 gates to 0; B = 0 leaves the D skip."""
+    rng = np.random.default_rng(seed)
+    batch, dim, N, L = 2, 3, 4, 20
+    A_log = rng.uniform(-0.5, 2.0, (dim, N))
+    delta = rng.normal(-2.0, 1.0, (batch, L, dim))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    D = rng.standard_normal(dim)
+    z = rng.standard_normal((batch, L, dim))
+    u1 = rng.standard_normal((batch, L, dim))
+    u2 = rng.standard_normal((batch, L, dim))
+    errs = []
+    o0, s0 = orc.selective_scan(np.zeros_like(u1), delta, A_log, B, C, D, z)
+    errs.append(float(np.max(np.abs(o0))) + float(np.max(np.abs(s0))))
+    o1, _ = orc.selective_scan(u1, delta, A_log, B, C, D, z)
+    o2, _ = orc.selective_scan(u2, delta, A_log, B, C, D, z)
+    o12, _ = orc.selective_scan(2.0 * u1 - 3.0 * u2, delta, A_log, B, C, D, z)
+    errs.append(rel_err(o12, 2.0 * o1 - 3.0 * o2))
+    t0 = 11
+    up = u1.copy()
+    up[:, t0] += 5.0
+    op, _ = orc.selective_scan(up, delta, A_log, B, C, D, z)
+    errs.append(float(np.max(np.abs(op[:, :t0] - o1[:, :t0]))))
+    errs.append(1.0 if np.max(np.abs(op[:, t0] - o1[:, t0])) == 0.0 else 0.0)
+    oz, _ = orc.selective_scan(u1, delta, A_log, B, C, D, np.zeros_like(z))
+    errs.append(float(np.max(np.abs(oz))))
+    ob, sb = orc.selective_scan(u1, delta, A_log, np.zeros_like(B), C, D, z)
+    errs.append(rel_err(ob, D * u1 * silu_ref(z)) + float(np.max(np.abs(sb))))
+    return max(errs)
+
+
+# name -> (function, tolerance)
+PINS = {
+    "zoh_matches_ode": (pin_zoh_matches_ode, 1e-10),
+    "lti_convolution": (pin_lti_convolution, 1e-11),
+    "n1_geometric": (pin_n1_geometric, 1e-12),
+    "theorem1_gated_rnn": (pin_theorem1_gated_rnn, 1e-12),
+    "small_dt_persists": (pin_small_dt_persists, 1e-14),
+    "large_dt_memoryless": (pin_large_dt_memoryless, 1e-12),
+    "brute_force": (pin_brute_force, 1e-11),
+    "associative_operator": (pin_associative_operator, 1e-12),
+    "continuation": (pin_continuation, 1e-12),
+    "structure": (pin_structure, 1e-12),
+}
