@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan hot path on B300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the selective scan of a layer (chunk load, discretisation, in-register
+recurrence, split-sequence carry when planned, fused epilogue) returning
+last_state, followed by one decode step on that state for the next token.
+
+Default workload: the Mamba-130M-shaped layer, B8 D1536 N16 L2048 bf16.
+Other workloads (--workload m1p4b|long|tiny) are available for exploration.
+
+Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
+instead (bounded samples of the same workload on the host cores).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_125_b300.workloads import (SCAN_CONFIGS, bf16_bits,  # noqa: E402
+                                                      make_config_inputs, make_decode_inputs)
+
+METRIC = "selective-scan channel-steps/s"
+L2_BYTES = 126 * 2**20
+FP32_LANES_PER_SM = 128          # FP32 lane-ops per clock per SM (B300)
+ALG_OPS_PER_STATE_STEP = 6       # FP32 ops per (channel, step, state) of the scan, see the design doc
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="m130", choices=sorted(SCAN_CONFIGS))
+    p.add_argument("--seed", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=100)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
+    p.add_argument("--lanes", type=int, default=0, help="plan override: lanes per channel")
+    p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
+    return p.parse_args()
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d.get("hbm_gbs", 6400.0), sm_max_mhz=d.get("sm_max_mhz", 2032.0), source="measured")
+    return dict(hbm_gbs=6400.0, sm_max_mhz=2032.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for ts, r in rows if t0 <= ts <= t1]
+        use = inside if inside else [r for ts, r in rows][-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in use if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for name, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ------------------------------------------------------------- our arm
+def run_ours(args, rank, world, device):
+    import torch
+    from selective_state_space_125_b300 import binding
+
+    cfg = SCAN_CONFIGS[args.workload]
+    B, Dm, N, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    es = 2 if cfg.dtype == "bf16" else 4
+    inp = make_config_inputs(cfg, seed=args.seed + rank)
+    tok = make_decode_inputs(B, Dm, N, cfg.dtype, seed=args.seed + 1000 + rank, pool=1)
+
+    def dev_x(a):
+        if cfg.dtype == "bf16":
+            return torch.from_numpy(bf16_bits(a).view(np.int16)).to(device).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    base = {k: dev_x(inp[k]) for k in ("u", "delta", "z", "B", "C")}
+    A_log, Dv, bias = f32(inp["A_log"]), f32(inp["D"]), f32(inp["delta_bias"])
+    base_tok = {k: dev_x(tok[k][0]) for k in ("u", "delta", "z", "B", "C")}
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + B * L * Dm * es
+    nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    sets = []
+    for i in range(nsets):
+        s = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        s["out"] = torch.empty((B, L, Dm), dtype=tdt, device=device)
+        s["last"] = torch.empty((B, Dm, N), dtype=torch.float32, device=device)
+        s["tok"] = {k: (v if i == 0 else v.clone()) for k, v in base_tok.items()}
+        s["tok_out"] = torch.empty((B, Dm), dtype=tdt, device=device)
+        sets.append(s)
+    plan = None
+    if args.lanes or args.segments:
+        plan = binding.ScanPlan(args.lanes, args.segments, 0)
+    chosen, scan_launches = binding.mamba_selective_scan_plan(B, Dm, N, L, cfg.dtype, plan)
+    stream = torch.cuda.current_stream(device)
+
+    def scan(s):
+        binding.mamba_selective_scan_fwd(s["u"], s["delta"], A_log, s["B"], s["C"], Dv, s["z"], bias,
+                                         s["out"], s["last"], plan=plan)
+
+    def decode(s):
+        t = s["tok"]
+        binding.mamba_selective_state_update(s["last"], t["u"], t["delta"], A_log, t["B"], t["C"], Dv, t["z"],
+                                             bias, s["tok_out"])
+
+    for i in range(args.warmup):
+        scan(sets[i % nsets])
+        decode(sets[i % nsets])
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    ev_scan = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(K):
+        s = sets[i % nsets]
+        ev_scan[i][0].record(stream)
+        scan(s)
+        ev_scan[i][1].record(stream)
+        decode(s)
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    assert binding.mamba_device_status() == 0, "a kernel reported a timeout"
+    ms_total = ev0.elapsed_time(ev1)
+    scan_ms = [a.elapsed_time(b) for a, b in ev_scan]
+    ms_per_step = ms_total / K
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+
+    chsteps = B * Dm * (L + 1)
+    value = world * chsteps / (ms_per_step / 1e3)
+
+    # ---- e2e through the public API with pinned host buffers
+    pin = {k: v.cpu().pin_memory() for k, v in base.items()}
+    pin_tok = {k: v.cpu().pin_memory() for k, v in base_tok.items()}
+    host_out = torch.empty((B, L, Dm), dtype=tdt).pin_memory()
+    host_tok_out = torch.empty((B, Dm), dtype=tdt).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pin.values()) + sum(
+        v.numel() * v.element_size() for v in pin_tok.values())
+    d2h = host_out.numel() * host_out.element_size() + host_tok_out.numel() * host_tok_out.element_size()
+    Ke = max(1, min(args.e2e_steps, K))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for i in range(Ke):
+        s = sets[i % nsets]
+        for k in pin:
+            s[k].copy_(pin[k], non_blocking=True)
+        for k in pin_tok:
+            s["tok"][k].copy_(pin_tok[k], non_blocking=True)
+        scan(s)
+        decode(s)
+        host_out.copy_(s["out"], non_blocking=True)
+        host_tok_out.copy_(s["tok_out"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    peaks = read_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    scan_avg_ms = float(np.mean(scan_ms))
+    alg_bytes = (4 * es * B * L * Dm + 2 * N * es * B * L + Dm * N * 4 + 2 * Dm * 4
+                 + (B * Dm * N * 4 if cfg.last_state else 0))
+    alg_ops = ALG_OPS_PER_STATE_STEP * N * B * L * Dm
+    achieved_gops = alg_ops / (scan_avg_ms / 1e3) / 1e9
+    peak_gops = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e9
+    achieved_gbs = alg_bytes / (scan_avg_ms / 1e3) / 1e9
+    clocks = sampler.summary(t_wall0, t_wall1)
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "scan_traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            tr = json.load(f).get(args.workload)
+        if tr and tr.get("plan") == [chosen.lanes_per_channel, chosen.segments]:
+            traffic = tr.get("dram_bytes_per_launch")
+    result = {
+        "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded numpy, see DESIGN.md)",
+        "config": {"workload": cfg.description, "batch": B, "d_inner": Dm, "d_state": N, "seqlen": L,
+                   "step": "scan(L tokens, last_state) + 1 decode step", "channel_steps_per_step": chsteps,
+                   "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB (> L2)",
+                   "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
+                            "tma": chosen.use_tma == 1}},
+        "roofline": {"bound": "alu", "achieved": achieved_gops, "peak": peak_gops, "unit": "Gop/s",
+                     "frac": achieved_gops / peak_gops, "traffic": traffic,
+                     "kernel": "selective scan call (all passes)", "kernel_ms": scan_avg_ms,
+                     "ops_per_launch": alg_ops,
+                     "peak_basis": f"{FP32_LANES_PER_SM} FP32 lanes x {sms} SMs x {peaks['sm_max_mhz']:.0f} MHz"},
+        "hbm": {"achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm_gbs"], "bytes_per_launch": alg_bytes,
+                "peak_source": f"MEASURED_PEAKS.json ({peaks['source']})"},
+        "e2e": {"value": world * chsteps / (e2e_ms / 1e3), "unit": "channel-steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": K * (scan_launches + 1),
+        "clocks": clocks,
+    }
+    return result
+
+
+# ------------------------------------------------- CPU oracle (baseline)
+def oracle_sample_rate(cfg, inp, seconds, threads):
+    """Oracle scan over the first k channels (all steps) of batch row 0, sized to ~seconds."""
+    import oracle
+    L, Dm = cfg.seqlen, cfg.dim
+
+    def run(k):
+        sl = slice(0, k)
+        t0 = time.perf_counter()
+        oracle.selective_scan(inp["u"][:1, :, sl], inp["delta"][:1, :, sl], inp["A_log"][sl], inp["B"][:1],
+                              inp["C"][:1], inp["D"][sl], inp["z"][:1, :, sl], inp["delta_bias"][sl],
+                              nthreads=threads)
+        return time.perf_counter() - t0
+
+    k = max(1, min(Dm, threads))
+    dt = run(k)
+    while dt < 0.5 and k < Dm:
+        k = min(Dm, k * 4)
+        dt = run(k)
+    per_ch = dt / k
+    k_final = max(1, min(Dm, int(seconds / per_ch)))
+    reps = max(1, int(seconds / (per_ch * k_final)))
+    total = 0.0
+    for _ in range(reps):
+        total += run(k_final)
+    rate = reps * k_final * L / total
+    return rate, f"oracle scan of {k_final} channels x {L} steps (batch row 0) x {reps}, {total:.1f} s"
+
+
+def cpu_baseline(args, cfg):
+    threads = os.cpu_count() or 1
+    inp = make_config_inputs(cfg, seed=args.seed)
+    rate, sample = oracle_sample_rate(cfg, inp, args.cpu_seconds, threads)
+    return {"value": rate, "unit": "channel-steps/s", "cores": threads, "kind": "oracle", "sample": sample}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on host cores, K timed steps of bounded samples."""
+    import oracle
+    cfg = SCAN_CONFIGS[args.workload]
+    threads = os.cpu_count() or 1
+    inp = make_config_inputs(cfg, seed=args.seed)
+    L, Dm = cfg.seqlen, cfg.dim
+    budget = 120.0 / max(1, args.steps + args.warmup)   # seconds per step
+    rate, _ = oracle_sample_rate(cfg, inp, min(2.0, budget), threads)
+    k = max(1, min(Dm, int(budget * rate / L)))
+    sl = slice(0, k)
+
+    def step():
+        oracle.selective_scan(inp["u"][:1, :, sl], inp["delta"][:1, :, sl], inp["A_log"][sl], inp["B"][:1],
+                              inp["C"][:1], inp["D"][sl], inp["z"][:1, :, sl], inp["delta_bias"][sl],
+                              nthreads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = k * L / dt
+    sample = f"oracle scan of {k} channels x {L} steps (batch row 0 of the {cfg.name} workload) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy)",
+        "config": {"workload": cfg.description, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "channel-steps/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "channel-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    from selective_state_space_125_b300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    result = run_ours(args, rank, world, device)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            result["cpu_baseline"] = cpu_baseline(args, SCAN_CONFIGS[args.workload])
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

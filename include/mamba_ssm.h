@@ -1,0 +1,187 @@
+/*
+ * mamba_ssm.h - C ABI of libmamba_ssm_b300.so, the B300 (sm_103a) selective
+ * state-space scan of Mamba and its single-token decode step.
+ *
+ * The operation (page titles and passages that define it):
+ *   "State Space Models and Mamba" (jonathanding.github.io, llm-learning)
+ *     §1   continuous system x' = A x + B u, y = C x + D u (D is the skip term);
+ *     §1.5 A is diagonal, stored as A_log, A = -exp(A_log);
+ *     §2   zero-order hold: Abar = exp(dt A), Bbar = A^-1 (exp(dt A) - I) B,
+ *          recurrence x_k = Abar x_{k-1} + Bbar u_k, y_k = C x_k;
+ *     §3   recurrence mode: one O(1) state update per token (decode);
+ *     §4   selectivity: dt_k = softplus(.), B_k and C_k change per step;
+ *          hardware-aware scan (paper §3.3.2): the (B,L,D,N) Abar/Bbar are
+ *          never written to memory, only y (B,L,D) is.
+ *   "Mamba" paper notes (awesome.papernotes.org, 2023_mamba)
+ *     "Design 1: Selective State Space": Bbar = (dt A)^-1 (exp(dt A) - I) dt B,
+ *     the selective_ssm sketch (y + D * x) and "Overall framework"
+ *     (out = y * SiLU(z)).
+ *
+ * Per batch b, channel d, state n and step t the scan computes
+ *     dt      = softplus(delta[b,t,d] + delta_bias[d])
+ *     A       = -exp(A_log[d,n])
+ *     h[n]    = exp(dt A) h[n] + (exp(dt A) - 1) / A * B[b,t,n] * u[b,t,d]
+ *     y       = sum_n C[b,t,n] h[n] + D[d] u[b,t,d]
+ *     out     = y * z / (1 + exp(-z))        (z = z[b,t,d]; no gate if z is NULL)
+ * from h = 0 (or from initial_state in the _ex entry point). The decode step
+ * is the same body for one token on a state kept in device memory.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller unless said otherwise;
+ *     tensors are contiguous, row-major, in the layouts given per argument.
+ *   - Work is enqueued on `stream` and is asynchronous: MAMBA_OK means the
+ *     arguments were valid and the kernels were launched. A fault inside a
+ *     kernel shows at the caller's next synchronisation, or through
+ *     mamba_device_status().
+ *   - Validation happens before any launch. Every failure returns a status
+ *     and sets a thread-local detail string (mamba_last_error_detail()).
+ *     No C++ exception crosses the ABI.
+ *   - `out` and `last_state` must not alias any input. The decode `state` is
+ *     read and written in place and must not alias any other argument.
+ *   - batch == 0, dim == 0 or (scan) seqlen == 0 is valid and empty: nothing
+ *     is read; a requested last_state is set to the initial state (zero).
+ *   - Input dtype: MAMBA_F32 or MAMBA_BF16 applies to u, delta, z, B, C and
+ *     out. A_log, D, delta_bias, states are always fp32. All arithmetic is
+ *     fp32 with fp32 state. With MAMBA_F32 inputs the kernels use accurate
+ *     expm1/exp/log1p; with MAMBA_BF16 inputs they use the hardware ex2/lg2
+ *     approximations (relative error of Bbar about 2^-22 / |dt A|).
+ *   - dstate (N) may be 1..256.
+ */
+#ifndef MAMBA_SSM_H
+#define MAMBA_SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(MAMBA_BUILDING_LIBRARY) && defined(__GNUC__)
+#define MAMBA_API __attribute__((visibility("default")))
+#else
+#define MAMBA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (a CUstream); NULL is the legacy default stream. */
+typedef struct CUstream_st *mamba_stream_t;
+
+typedef enum {
+    MAMBA_F32 = 0,
+    MAMBA_BF16 = 1
+} mamba_dtype_t;
+
+typedef enum {
+    MAMBA_OK = 0,
+    MAMBA_ERR_INVALID_ARG = 1,   /* NULL required pointer, negative size, aliasing */
+    MAMBA_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (e.g. N > 256) */
+    MAMBA_ERR_CUDA = 3,          /* a CUDA runtime call failed; detail names it */
+    MAMBA_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (see mamba_device_status) */
+} mamba_status_t;
+
+/*
+ * Selective scan, forward.
+ *   batch, dim, dstate, seqlen : B, D (= d_inner), N (= d_state), L.
+ *   in_dtype   : dtype of u, delta, z, B, C and out.
+ *   u          : (B, L, D) input x of the SSM.
+ *   delta      : (B, L, D) pre-softplus step (dt = softplus(delta + delta_bias)).
+ *   A_log      : (D, N) fp32; A = -exp(A_log).
+ *   B, C       : (B, L, N) input and output projections, shared by all D channels of a batch row.
+ *   D          : (D,) fp32 skip weights, or NULL for no skip.
+ *   z          : (B, L, D) gate input, or NULL for no gate.
+ *   delta_bias : (D,) fp32, or NULL for zero.
+ *   out        : (B, L, D) written.
+ *   last_state : (B, D, N) fp32 written with h after step L-1, or NULL.
+ * Splitting long sequences over several CTAs uses a temporary stream-ordered
+ * workspace (cudaMallocAsync / cudaFreeAsync on `stream`, about
+ * B * D * (N + 1) * 4 bytes per extra segment); MAMBA_ERR_CUDA if it cannot
+ * be had.
+ */
+MAMBA_API mamba_status_t mamba_selective_scan_fwd(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+    const void *u, const void *delta, const float *A_log,
+    const void *B, const void *C, const float *D, const void *z,
+    const float *delta_bias, void *out, float *last_state,
+    mamba_stream_t stream);
+
+/*
+ * Plan knobs for mamba_selective_scan_fwd_ex. A zero field means "choose
+ * automatically"; results never depend on the plan beyond fp32 rounding
+ * order (the tests compare plans against each other and the oracle).
+ *   lanes_per_channel : threads sharing one channel's N states: a power of
+ *                       two from ceil(N / 16) to 16;
+ *   segments          : the sequence is cut into this many time segments that
+ *                       run in parallel, joined by the two-pass carry (1 = off);
+ *   use_tma           : 0 auto, 1 require the TMA tile loader (error if the
+ *                       layout does not allow it), 2 force plain loads.
+ */
+typedef struct {
+    int lanes_per_channel;
+    int segments;
+    int use_tma;
+} mamba_scan_plan_t;
+
+/*
+ * As mamba_selective_scan_fwd, plus:
+ *   initial_state : (B, D, N) fp32 state to start from, or NULL for zero
+ *                   (lets a prefill continue from an earlier chunk or a decode state);
+ *   plan          : NULL or knobs above.
+ */
+MAMBA_API mamba_status_t mamba_selective_scan_fwd_ex(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+    const void *u, const void *delta, const float *A_log,
+    const void *B, const void *C, const float *D, const void *z,
+    const float *delta_bias, const float *initial_state, void *out,
+    float *last_state, const mamba_scan_plan_t *plan, mamba_stream_t stream);
+
+/*
+ * The plan mamba_selective_scan_fwd_ex would use for these sizes on the
+ * current device, assuming 16-byte aligned pointers: writes the chosen knobs
+ * to *chosen (use_tma = 1 if the TMA loader would be used, else 2) and the
+ * number of kernel launches one call makes (1, or 2 with segments > 1) to
+ * *kernel_launches. Validation and errors as for the scan itself.
+ */
+MAMBA_API mamba_status_t mamba_selective_scan_plan(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+    const mamba_scan_plan_t *plan, mamba_scan_plan_t *chosen, int *kernel_launches);
+
+/*
+ * Single-token decode step on a resident state ("State Space Models and
+ * Mamba" §3, recurrence mode).
+ *   state      : (B, D, N) fp32, read and written in place.
+ *   u, delta, z: (B, D) in_dtype (z may be NULL).
+ *   A_log      : (D, N) fp32.
+ *   B, C       : (B, N) in_dtype.
+ *   D, delta_bias : (D,) fp32 or NULL.
+ *   out        : (B, D) in_dtype, written.
+ * Always uses the accurate expm1/exp/log1p path: the step is bound by the
+ * state's memory traffic, so the accurate math costs nothing measurable.
+ */
+MAMBA_API mamba_status_t mamba_selective_state_update(
+    int batch, int dim, int dstate, mamba_dtype_t in_dtype,
+    float *state, const void *u, const void *delta, const float *A_log,
+    const void *B, const void *C, const float *D, const void *z,
+    const float *delta_bias, void *out, mamba_stream_t stream);
+
+/* Static description of a status code. */
+MAMBA_API const char *mamba_status_string(mamba_status_t s);
+
+/* Detail of the last failure on the calling host thread ("" if none). */
+MAMBA_API const char *mamba_last_error_detail(void);
+
+/*
+ * Kernel-side status word of the current device. Kernels never trap; a
+ * bounded wait that runs out records MAMBA_ERR_TIMEOUT here and the kernel
+ * returns early. This call synchronises `stream`, copies the word to
+ * *status_out and clears it.
+ */
+MAMBA_API mamba_status_t mamba_device_status(int *status_out, mamba_stream_t stream);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+MAMBA_API int mamba_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SSM_H */

@@ -1,0 +1,435 @@
+// C ABI of libmamba_ssm_b300.so (declared in include/mamba_ssm.h): argument
+// validation, work planning, TMA descriptor encoding and kernel dispatch.
+// Every step of the computation runs in the kernels of scan_kernel.cuh and
+// state_update.cu; this file only checks, plans and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "mamba_ssm.h"
+#include "scan_args.h"
+
+namespace mamba {
+cudaError_t launch_scan_f32(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_bf16(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+bool scan_variant_f32(int, int, ScanVariant*);
+bool scan_variant_bf16(int, int, ScanVariant*);
+}  // namespace mamba
+
+using namespace mamba;
+
+// Kernel status word, one instance per device (see mamba_device_status).
+__device__ int g_mamba_status_word;
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kMaxState = 256;
+constexpr int kMaxDevices = 64;
+
+thread_local std::string t_detail;
+
+mamba_status_t fail(mamba_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_detail = buf;
+  return s;
+}
+
+mamba_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(MAMBA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device facts, read once with the device current.
+mamba_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MAMBA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&di.status), g_mamba_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    di.ready = true;
+  }
+  *out = di;
+  return MAMBA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D map over a row-major (outer, mid, inner) tensor with box (box_inner, box_mid, 1).
+mamba_status_t encode_3d(CUtensorMap* map, const void* base, int es, uint64_t inner, uint64_t mid, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_mid) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {inner, mid, outer};
+  const cuuint64_t strides[2] = {inner * es, inner * mid * es};
+  const cuuint32_t box[3] = {box_inner, box_mid, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = (es == 2) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MAMBA_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult %d", int(r));
+  return MAMBA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bool variant_for(int dtype, int npl, int lpc, ScanVariant* v) {
+  return dtype == 0 ? scan_variant_f32(npl, lpc, v) : scan_variant_bf16(npl, lpc, v);
+}
+
+// States per thread for `lpc` threads per channel: the smallest of 4, 8, 16
+// that covers N; 0 if none does.
+int npl_for(int N, int lpc) {
+  for (int npl : {4, 8, 16})
+    if (npl * lpc >= N) return npl;
+  return 0;
+}
+
+// Threads the planner aims to keep resident (12 warps per SM).
+constexpr int kTargetThreadsPerSM = 384;
+
+struct Plan {
+  int npl, lpc, nseg, seg_len, chunk;
+  bool tma_x, tma_bc;
+};
+
+mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamba_scan_plan_t* knobs, int sms,
+                         const void* u, const void* delta, const void* z, const void* Bp, const void* Cp,
+                         Plan* plan) {
+  const int es = dtype == 0 ? 4 : 2;
+  int lpc_min = 1;
+  while (lpc_min * 16 < N) lpc_min *= 2;
+  int lpc = knobs ? knobs->lanes_per_channel : 0;
+  const long long channels = (long long)batch * dim;
+  const long long target = (long long)sms * kTargetThreadsPerSM;
+  if (lpc == 0) {
+    // Spread a channel's states over more threads while that is needed to
+    // fill the device, as long as each thread keeps at least 4 real states.
+    lpc = lpc_min;
+    ScanVariant probe;
+    while (channels * lpc < target && lpc * 2 <= 16 && N >= 4 * lpc * 2 &&
+           variant_for(dtype, npl_for(N, lpc * 2), lpc * 2, &probe))
+      lpc *= 2;
+  }
+  if (lpc < lpc_min || (lpc & (lpc - 1)) != 0 || lpc > 16)
+    return fail(MAMBA_ERR_INVALID_ARG, "lanes_per_channel=%d is not a power of two in [%d, 16] for N=%d", lpc,
+                lpc_min, N);
+  const int npl = npl_for(N, lpc);
+  ScanVariant v;
+  if (npl == 0 || !variant_for(dtype, npl, lpc, &v))
+    return fail(MAMBA_ERR_UNSUPPORTED, "no scan kernel for N=%d with lanes_per_channel=%d", N, lpc);
+
+  int nseg = knobs ? knobs->segments : 0;
+  const int max_seg = std::max(1, std::min(65535, (L + v.chunk - 1) / v.chunk));
+  if (nseg == 0) {
+    const long long threads = channels * lpc;
+    nseg = 1;
+    if (threads < target) nseg = int((target + threads - 1) / threads);
+    // keep at least 8 chunks per segment, at most 64 segments
+    nseg = std::min({nseg, 64, std::max(1, L / (8 * v.chunk))});
+  }
+  if (nseg < 1) return fail(MAMBA_ERR_INVALID_ARG, "segments=%d must be >= 1", nseg);
+  nseg = std::min(nseg, max_seg);
+  int seg_len = (L + nseg - 1) / nseg;
+  seg_len = (seg_len + v.chunk - 1) / v.chunk * v.chunk;
+  nseg = (L + seg_len - 1) / seg_len;  // every segment non-empty
+
+  const int cb = kScanThreads / lpc;
+  const bool x_ok = ((long long)dim * es) % 16 == 0 && aligned16(u) && aligned16(delta) && (!z || aligned16(z)) &&
+                    (cb * es) % 16 == 0;
+  const bool bc_ok = ((long long)N * es) % 16 == 0 && aligned16(Bp) && aligned16(Cp);
+  const int use_tma = knobs ? knobs->use_tma : 0;
+  if (use_tma == 1 && !(x_ok && bc_ok))
+    return fail(MAMBA_ERR_INVALID_ARG,
+                "use_tma=1 but the layout does not allow TMA tiles (needs 16-byte aligned pointers, "
+                "dim*%d and dstate*%d multiples of 16 bytes)", es, es);
+  plan->npl = npl;
+  plan->lpc = lpc;
+  plan->nseg = nseg;
+  plan->seg_len = seg_len;
+  plan->chunk = v.chunk;
+  plan->tma_x = use_tma != 2 && x_ok;
+  plan->tma_bc = use_tma != 2 && bc_ok;
+  return MAMBA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                           const void* u, const void* delta, const float* A_log, const void* B,
+                                           const void* C, const float* D, const void* z, const float* delta_bias,
+                                           const float* initial_state, void* out, float* last_state,
+                                           const mamba_scan_plan_t* plan_knobs, mamba_stream_t stream_) {
+  t_detail.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 0 || dim < 0 || seqlen < 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
+  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
+  if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
+  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
+  if (plan_knobs && (plan_knobs->lanes_per_channel < 0 || plan_knobs->segments < 0 || plan_knobs->use_tma < 0 ||
+                     plan_knobs->use_tma > 2))
+    return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
+  if (batch == 0 || dim == 0) return MAMBA_OK;
+  const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
+  const size_t es = dtype == 0 ? 4 : 2;
+  const size_t n_state = (size_t)batch * dim * dstate;
+  if (!A_log) return fail(MAMBA_ERR_INVALID_ARG, "A_log is NULL");
+  if (seqlen == 0) {
+    if (last_state) {
+      cudaError_t e = initial_state
+                          ? cudaMemcpyAsync(last_state, initial_state, n_state * 4, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(last_state, 0, n_state * 4, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "empty-sequence last_state");
+    }
+    return MAMBA_OK;
+  }
+  if (!u || !delta || !B || !C || !out)
+    return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL (u=%p delta=%p B=%p C=%p out=%p)", u, delta, B, C,
+                out);
+  const size_t nx = (size_t)batch * seqlen * dim * es;
+  const size_t nbc = (size_t)batch * seqlen * dstate * es;
+  const void* inputs[] = {u, delta, z, B, C, A_log, D, delta_bias, initial_state};
+  const size_t sizes[] = {nx, nx, nx, nbc, nbc, (size_t)dim * dstate * 4, (size_t)dim * 4, (size_t)dim * 4,
+                          n_state * 4};
+  for (int i = 0; i < 9; ++i) {
+    if (overlaps(out, nx, inputs[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "out aliases input %d", i);
+    if (overlaps(last_state, n_state * 4, inputs[i], sizes[i]))
+      return fail(MAMBA_ERR_INVALID_ARG, "last_state aliases input %d", i);
+  }
+  if (overlaps(out, nx, last_state, n_state * 4)) return fail(MAMBA_ERR_INVALID_ARG, "out aliases last_state");
+
+  DeviceInfo di;
+  mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  Plan plan;
+  st = make_plan(dtype, batch, dim, dstate, seqlen, plan_knobs, di.sms, u, delta, z, B, C, &plan);
+  if (st != MAMBA_OK) return st;
+
+  ScanMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const uint32_t cb = uint32_t(kScanThreads / plan.lpc);
+  if (plan.tma_x) {
+    if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+    if ((st = encode_3d(&maps.delta, delta, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+    if (z && (st = encode_3d(&maps.z, z, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+  }
+  if (plan.tma_bc) {
+    if ((st = encode_3d(&maps.B, B, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
+    if ((st = encode_3d(&maps.C, C, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
+  }
+
+  ScanArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.batch = batch;
+  a.dim = dim;
+  a.dstate = dstate;
+  a.seqlen = seqlen;
+  a.nseg = plan.nseg;
+  a.seg_len = plan.seg_len;
+  a.u = u;
+  a.delta = delta;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.A_log = A_log;
+  a.D = D;
+  a.delta_bias = delta_bias;
+  a.h0 = initial_state;
+  a.out = out;
+  a.last_state = last_state;
+  a.tma_x = plan.tma_x;
+  a.tma_bc = plan.tma_bc;
+  a.status = di.status;
+
+  auto launch = [&](ScanMode mode, unsigned nz) {
+    dim3 grid((dim + cb - 1) / cb, batch, nz);
+    return dtype == 0 ? launch_scan_f32(plan.npl, plan.lpc, mode, a, maps, grid, stream)
+                      : launch_scan_bf16(plan.npl, plan.lpc, mode, a, maps, grid, stream);
+  };
+
+  void* work = nullptr;
+  if (plan.nseg > 1) {
+    const size_t rows = (size_t)batch * (plan.nseg - 1) * dim;
+    const size_t bytes = rows * (dstate + 1) * sizeof(float);
+    cudaError_t e = cudaMallocAsync(&work, bytes, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(split-sequence workspace)");
+    a.agg_h = static_cast<float*>(work);
+    a.agg_dsum = a.agg_h + rows * dstate;
+    e = launch(ScanMode::kAggregate, plan.nseg - 1);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(work, stream);
+      return cuda_fail(e, "scan aggregate pass launch");
+    }
+  }
+  cudaError_t e = launch(ScanMode::kFull, plan.nseg);
+  if (work) {
+    cudaError_t e2 = cudaFreeAsync(work, stream);
+    if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync(split-sequence workspace)");
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "scan launch");
+  return MAMBA_OK;
+}
+
+mamba_status_t mamba_selective_scan_plan(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                         const mamba_scan_plan_t* knobs, mamba_scan_plan_t* chosen,
+                                         int* kernel_launches) {
+  t_detail.clear();
+  if (!chosen || !kernel_launches) return fail(MAMBA_ERR_INVALID_ARG, "chosen / kernel_launches is NULL");
+  if (batch <= 0 || dim <= 0 || seqlen <= 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "sizes must be positive (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
+  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
+  if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
+  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  DeviceInfo di;
+  mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  Plan plan;
+  const void* aligned = reinterpret_cast<const void*>(uintptr_t(256));
+  st = make_plan(in_dtype == MAMBA_F32 ? 0 : 1, batch, dim, dstate, seqlen, knobs, di.sms, aligned, aligned,
+                 aligned, aligned, aligned, &plan);
+  if (st != MAMBA_OK) return st;
+  chosen->lanes_per_channel = plan.lpc;
+  chosen->segments = plan.nseg;
+  chosen->use_tma = (plan.tma_x && plan.tma_bc) ? 1 : 2;
+  *kernel_launches = plan.nseg > 1 ? 2 : 1;
+  return MAMBA_OK;
+}
+
+mamba_status_t mamba_selective_scan_fwd(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                        const void* u, const void* delta, const float* A_log, const void* B,
+                                        const void* C, const float* D, const void* z, const float* delta_bias,
+                                        void* out, float* last_state, mamba_stream_t stream) {
+  return mamba_selective_scan_fwd_ex(batch, dim, dstate, seqlen, in_dtype, u, delta, A_log, B, C, D, z, delta_bias,
+                                     nullptr, out, last_state, nullptr, stream);
+}
+
+mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamba_dtype_t in_dtype, float* state,
+                                            const void* u, const void* delta, const float* A_log, const void* B,
+                                            const void* C, const float* D, const void* z, const float* delta_bias,
+                                            void* out, mamba_stream_t stream_) {
+  t_detail.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 0 || dim < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d)", batch, dim);
+  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
+  if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
+  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  if (batch == 0 || dim == 0) return MAMBA_OK;
+  if (!state || !u || !delta || !A_log || !B || !C || !out)
+    return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL");
+  const size_t es = in_dtype == MAMBA_F32 ? 4 : 2;
+  const size_t ns = (size_t)batch * dim * dstate * 4;
+  const size_t nx = (size_t)batch * dim * es;
+  const size_t nbc = (size_t)batch * dstate * es;
+  const void* others[] = {u, delta, z, B, C, A_log, D, delta_bias, out};
+  const size_t sizes[] = {nx, nx, nx, nbc, nbc, (size_t)dim * dstate * 4, (size_t)dim * 4, (size_t)dim * 4, nx};
+  for (int i = 0; i < 9; ++i)
+    if (overlaps(state, ns, others[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "state aliases argument %d", i);
+  for (int i = 0; i < 8; ++i)
+    if (overlaps(out, nx, others[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "out aliases input %d", i);
+  DecodeArgs a;
+  a.batch = batch;
+  a.dim = dim;
+  a.dstate = dstate;
+  a.state = state;
+  a.u = u;
+  a.delta = delta;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.A_log = A_log;
+  a.D = D;
+  a.delta_bias = delta_bias;
+  a.out = out;
+  cudaError_t e = launch_state_update(in_dtype == MAMBA_F32 ? 0 : 1, a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "state update launch");
+  return MAMBA_OK;
+}
+
+const char* mamba_status_string(mamba_status_t s) {
+  switch (s) {
+    case MAMBA_OK: return "ok";
+    case MAMBA_ERR_INVALID_ARG: return "invalid argument";
+    case MAMBA_ERR_UNSUPPORTED: return "unsupported";
+    case MAMBA_ERR_CUDA: return "CUDA error";
+    case MAMBA_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* mamba_last_error_detail(void) { return t_detail.c_str(); }
+
+mamba_status_t mamba_device_status(int* status_out, mamba_stream_t stream_) {
+  t_detail.clear();
+  if (!status_out) return fail(MAMBA_ERR_INVALID_ARG, "status_out is NULL");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  DeviceInfo di;
+  mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, di.status, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(di.status, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status word");
+  *status_out = word;
+  return MAMBA_OK;
+}
+
+int mamba_version(void) { return kVersion; }
+
+}  // extern "C"

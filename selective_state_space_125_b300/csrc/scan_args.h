@@ -1,0 +1,71 @@
+// Host/device argument blocks and launcher declarations shared by api.cu and
+// the kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace mamba {
+
+constexpr int kScanThreads = 128;   // threads per CTA of the scan kernels
+constexpr int kScanStages = 3;      // TMA pipeline depth (time chunks in flight)
+
+struct ScanArgs {
+  int batch, dim, dstate, seqlen;
+  int nseg;        // time segments run in parallel (1 = whole sequence per CTA)
+  int seg_len;     // steps per segment (a multiple of the chunk length)
+  const void* u;   // (B, L, D)
+  const void* delta;
+  const void* z;   // may be null
+  const void* B;   // (B, L, N)
+  const void* C;
+  const float* A_log;       // (D, N)
+  const float* D;           // (D) or null
+  const float* delta_bias;  // (D) or null
+  const float* h0;          // (B, D, N) or null
+  void* out;                // (B, L, D)
+  float* last_state;        // (B, D, N) or null
+  float* agg_h;             // (B, nseg-1, D, N): segment end state started from zero
+  float* agg_dsum;          // (B, nseg-1, D): sum of dt over the segment
+  int tma_x;                // u/delta/z tiles by TMA (else plain loads)
+  int tma_bc;               // B/C tiles by TMA (else plain loads)
+  int* status;              // device status word (see record_status)
+};
+
+struct ScanMaps {
+  CUtensorMap u, delta, z, B, C;
+};
+
+// Geometry of one kernel variant, for the planner.
+struct ScanVariant {
+  int npl;     // states per thread
+  int lpc;     // threads per channel
+  int chunk;   // time steps per pipeline stage
+  size_t smem_bytes;
+};
+
+enum class ScanMode { kFull = 0, kAggregate = 1 };
+
+// Launches one scan pass. Returns cudaSuccess or the launch error.
+// dtype: 0 = fp32 inputs (precise math), 1 = bf16 inputs (fast math).
+cudaError_t launch_scan(int dtype, int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps,
+                        dim3 grid, cudaStream_t stream);
+
+
+// Decode step.
+struct DecodeArgs {
+  int batch, dim, dstate;
+  float* state;
+  const void* u;
+  const void* delta;
+  const void* z;
+  const void* B;
+  const void* C;
+  const float* A_log;
+  const float* D;
+  const float* delta_bias;
+  void* out;
+};
+cudaError_t launch_state_update(int dtype, const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace mamba

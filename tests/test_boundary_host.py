@@ -1,0 +1,110 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments before any CUDA call. Nothing here launches a kernel or
+touches a device (all pointers are fake and every case fails validation)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mamba_ssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selective_state_space_125_b300 import build, binding
+    build.build()
+    return binding.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MAMBA_API\s+[\w\s\*]*?\b(mamba_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for required in ("mamba_selective_scan_fwd", "mamba_selective_state_update"):
+        assert required in names
+    from selective_state_space_125_b300 import binding
+    assert sorted(binding.EXPORTED) == names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def test_only_the_abi_is_exported():
+    from selective_state_space_125_b300 import binding
+    out = os.popen(f"nm -D --defined-only {binding.LIB_PATH}").read().split("\n")
+    names = {line.split()[-1] for line in out if line.strip() and " T " in line}
+    assert {n for n in names if n.startswith("mamba_")} == set(declared_symbols())
+
+
+def test_version_and_strings(lib):
+    assert lib.mamba_version() >= 10000
+    for code, word in [(0, b"ok"), (1, b"invalid"), (2, b"unsupported"), (3, b"CUDA"), (4, b"timed out")]:
+        assert word in lib.mamba_status_string(code)
+
+
+FAKE = 0x7F0000000000  # never dereferenced: every call below fails validation
+
+
+def scan(lib, batch=2, dim=8, dstate=16, seqlen=4, dtype=1, u=FAKE, delta=FAKE + 0x100000,
+         A_log=FAKE + 0x200000, B=FAKE + 0x300000, C=FAKE + 0x400000, D=None, z=None, bias=None,
+         h0=None, out=FAKE + 0x500000, last=None, plan=None):
+    return lib.mamba_selective_scan_fwd_ex(batch, dim, dstate, seqlen, dtype, u, delta, A_log, B, C, D,
+                                           z, bias, h0, out, last, plan, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=-1), 1), (dict(dim=-3), 1), (dict(seqlen=-1), 1), (dict(dstate=0), 1),
+    (dict(dstate=257), 2), (dict(dtype=7), 1), (dict(batch=70000), 2),
+    (dict(u=None), 1), (dict(delta=None), 1), (dict(B=None), 1), (dict(C=None), 1),
+    (dict(out=None), 1), (dict(A_log=None), 1),
+    (dict(out=FAKE), 1),                                   # out aliases u
+    (dict(last=FAKE + 0x300000 + 8), 1),                   # last_state aliases B
+])
+def test_scan_rejects_bad_arguments(lib, kw, status):
+    assert scan(lib, **kw) == status
+    assert lib.mamba_last_error_detail() != b""
+
+
+def test_bad_plan_knobs(lib):
+    from selective_state_space_125_b300.binding import ScanPlan
+    for p in (ScanPlan(-1, 0, 0), ScanPlan(0, -2, 0), ScanPlan(0, 0, 3)):
+        assert scan(lib, plan=ctypes.byref(p)) == 1
+
+
+def test_empty_problems_are_ok_without_a_device(lib):
+    # batch == 0 or dim == 0: nothing to do, no CUDA call is made.
+    assert scan(lib, batch=0) == 0
+    assert scan(lib, dim=0) == 0
+    assert lib.mamba_selective_state_update(0, 8, 16, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                            None, None, None, FAKE + 0x900000, None) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(batch=-1), 1), (dict(dstate=0), 1), (dict(dstate=300), 2), (dict(dtype=5), 1),
+    (dict(state=None), 1), (dict(u=None), 1), (dict(out=None), 1),
+    (dict(out=FAKE), 1),                                   # out aliases state
+])
+def test_state_update_rejects_bad_arguments(lib, kw, status):
+    a = dict(batch=2, dim=8, dstate=16, dtype=1, state=FAKE, u=FAKE + 0x100000, delta=FAKE + 0x200000,
+             A_log=FAKE + 0x300000, B=FAKE + 0x400000, C=FAKE + 0x500000, out=FAKE + 0x600000)
+    a.update(kw)
+    assert lib.mamba_selective_state_update(a["batch"], a["dim"], a["dstate"], a["dtype"], a["state"], a["u"],
+                                            a["delta"], a["A_log"], a["B"], a["C"], None, None, None,
+                                            a["out"], None) == status
+
+
+def test_binding_rejects_host_tensors():
+    torch = pytest.importorskip("torch")
+    from selective_state_space_125_b300 import binding
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        binding.mamba_selective_scan_fwd(x, x, torch.zeros(8, 16), torch.zeros(1, 4, 16), torch.zeros(1, 4, 16))
+    with pytest.raises(TypeError):
+        binding.mamba_selective_scan_fwd(x.double(), x, torch.zeros(8, 16), x, x)

@@ -1,0 +1,191 @@
+"""GPU parity of the selective scan against the fp64 oracle, through the C ABI.
+
+Tolerances (max relative error with an rms floor, see helpers.parity_err):
+1e-4 for fp32 inputs and 2e-2 for bf16 inputs; fp32 state on the GPU.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import TOL, parity_err, to_numpy, to_torch, upload_scan
+from selective_state_space_125_b300.workloads import SCAN_CONFIGS, make_config_inputs, make_scan_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_125_b300 import build
+    build.build()
+    return torch.device("cuda:0")
+
+
+def run_gpu(inp, dev, plan=None, with_z=True, with_D=True, with_bias=True, h0=None):
+    import torch
+    from selective_state_space_125_b300 import binding
+    t = upload_scan(inp, dev, with_z, with_D, with_bias)
+    h0t = None if h0 is None else torch.from_numpy(np.ascontiguousarray(h0, np.float32)).to(dev)
+    out, last = binding.mamba_selective_scan_fwd(
+        t["u"], t["delta"], t["A_log"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+        return_last_state=True, initial_state=h0t, plan=plan)
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    return to_numpy(out), to_numpy(last)
+
+
+def run_oracle(inp, with_z=True, with_D=True, with_bias=True, h0=None):
+    return oracle.selective_scan(inp["u"], inp["delta"], inp["A_log"], inp["B"], inp["C"],
+                                 inp["D"] if with_D else None, inp["z"] if with_z else None,
+                                 inp["delta_bias"] if with_bias else None, h0=h0)
+
+
+def assert_parity(got, ref, dtype, what=""):
+    out, last = got
+    rout, rlast = ref
+    e1, e2 = parity_err(out, rout), parity_err(last, rlast)
+    assert e1 <= TOL[dtype] and e2 <= TOL[dtype], f"{what}: out err {e1:.2e}, last_state err {e2:.2e}"
+    return e1, e2
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_fp32_config(dev, seed):
+    inp = make_config_inputs(SCAN_CONFIGS["tiny"], seed)
+    assert_parity(run_gpu(inp, dev), run_oracle(inp), "f32", f"tiny seed {seed}")
+
+
+# Several tiles along D and L, a ragged tail in both, both loaders.
+SHAPES = [
+    (2, 256, 16, 333),    # TMA tiles, ragged L
+    (2, 200, 16, 97),     # dim*2 % 16 != 0 for bf16 -> plain loads, ragged D and L
+    (1, 136, 16, 1),      # L = 1
+    (3, 64, 16, 64),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_shapes_auto_plan(dev, dtype, shape):
+    batch, dim, dstate, seqlen = shape
+    inp = make_scan_inputs(batch, dim, dstate, seqlen, dtype, seed=11)
+    assert_parity(run_gpu(inp, dev), run_oracle(inp), dtype, f"{shape} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lpc", [1, 2, 4])
+@pytest.mark.parametrize("segments", [1, 2, 3, 7])
+def test_plans_agree_with_oracle(dev, dtype, lpc, segments):
+    inp = make_scan_inputs(2, 160, 16, 1000, dtype, seed=5, dt_range=(1e-4, 1.0))
+    ref = run_oracle(inp)
+    got = run_gpu(inp, dev, plan=dict(lanes_per_channel=lpc, segments=segments, use_tma=0))
+    assert_parity(got, ref, dtype, f"lpc={lpc} segments={segments}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("use_tma", [1, 2])
+def test_tma_and_plain_loaders_agree(dev, dtype, use_tma):
+    inp = make_scan_inputs(2, 256, 16, 200, dtype, seed=6)
+    got = run_gpu(inp, dev, plan=dict(lanes_per_channel=0, segments=0, use_tma=use_tma))
+    assert_parity(got, run_oracle(inp), dtype, f"use_tma={use_tma}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [1, 3, 4, 8, 12, 32, 64, 128, 256])
+def test_state_sizes(dev, dtype, dstate):
+    inp = make_scan_inputs(2, 48, dstate, 70, dtype, seed=dstate)
+    assert_parity(run_gpu(inp, dev), run_oracle(inp), dtype, f"N={dstate}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(with_z=False), dict(with_D=False), dict(with_bias=False),
+                                  dict(with_z=False, with_D=False, with_bias=False)])
+def test_optional_arguments(dev, dtype, opts):
+    inp = make_scan_inputs(2, 64, 16, 90, dtype, seed=3)
+    assert_parity(run_gpu(inp, dev, **opts), run_oracle(inp, **opts), dtype, str(opts))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("segments", [1, 3])
+def test_initial_state_continues_a_scan(dev, dtype, segments):
+    inp = make_scan_inputs(2, 96, 16, 300, dtype, seed=8)
+    L1 = 130
+    first = {k: (v[:, :L1] if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
+    second = {k: (v[:, L1:] if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
+    o1, s1 = run_gpu(first, dev)
+    plan = dict(lanes_per_channel=0, segments=segments, use_tma=0)
+    o2, s2 = run_gpu(second, dev, plan=plan, h0=s1)
+    ref_out, ref_last = run_oracle(inp)
+    assert_parity((np.concatenate([o1, o2], 1), s2), (ref_out, ref_last), dtype, "continuation")
+    # and against the oracle started from the same GPU state (isolates the second call)
+    assert_parity((o2, s2), run_oracle(second, h0=s1), dtype, "continuation, second call")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_small_and_large_dt_limits(dev, dtype):
+    """delta + bias = -40: the initial state persists and y = C h0 + D u ("persist & ignore");
+    delta + bias = +40: the state forgets h0 and y is memoryless ("reset & focus")."""
+    inp = make_scan_inputs(1, 64, 16, 64, dtype, seed=4)
+    h0 = np.random.default_rng(4).standard_normal((1, 64, 16)).astype(np.float32)
+    for value in (-40.0, 40.0):
+        x = dict(inp)
+        x["delta"] = np.full_like(inp["delta"], value)
+        x["delta_bias"] = np.zeros_like(inp["delta_bias"])
+        got = run_gpu(x, dev, h0=h0, plan=dict(lanes_per_channel=0, segments=0, use_tma=0))
+        assert_parity(got, run_oracle(x, h0=h0), dtype, f"delta={value}")
+        if value < 0:
+            assert parity_err(got[1], h0) <= TOL[dtype]
+
+
+def test_empty_sequence_sets_last_state(dev):
+    import torch
+    from selective_state_space_125_b300 import binding
+    u = torch.zeros(2, 0, 32, dtype=torch.bfloat16, device=dev)
+    bc = torch.zeros(2, 0, 16, dtype=torch.bfloat16, device=dev)
+    A_log = torch.zeros(32, 16, device=dev)
+    h0 = torch.randn(2, 32, 16, device=dev)
+    out, last = binding.mamba_selective_scan_fwd(u, u, A_log, bc, bc, initial_state=h0, return_last_state=True)
+    torch.cuda.synchronize()
+    assert out.numel() == 0 and torch.equal(last, h0)
+    _, last0 = binding.mamba_selective_scan_fwd(u, u, A_log, bc, bc, return_last_state=True)
+    assert torch.count_nonzero(last0).item() == 0
+
+
+def test_plan_errors_raise(dev):
+    from selective_state_space_125_b300 import binding
+    inp = make_scan_inputs(1, 60, 16, 40, "bf16", seed=1)   # dim*2 = 120 bytes: no TMA
+    with pytest.raises(binding.MambaError):
+        run_gpu(inp, dev, plan=dict(lanes_per_channel=0, segments=0, use_tma=1))
+    with pytest.raises(binding.MambaError):
+        run_gpu(inp, dev, plan=dict(lanes_per_channel=3, segments=0, use_tma=0))
+
+
+# ---- full-size workloads: sampled channels against the oracle, computed one by one
+def sampled_oracle(inp, bs, ds):
+    sub = {}
+    for k in ("u", "delta", "z"):
+        sub[k] = inp[k][bs][:, :, ds]
+    for k in ("B", "C"):
+        sub[k] = inp[k][bs]
+    sub["A_log"] = inp["A_log"][ds]
+    sub["D"] = inp["D"][ds]
+    sub["delta_bias"] = inp["delta_bias"][ds]
+    return oracle.selective_scan(sub["u"], sub["delta"], sub["A_log"], sub["B"], sub["C"], sub["D"],
+                                 sub["z"], sub["delta_bias"])
+
+
+@pytest.mark.parametrize("name", ["m130", "m1p4b", "long"])
+def test_full_size_configs_sampled(dev, name):
+    cfg = SCAN_CONFIGS[name]
+    inp = make_config_inputs(cfg, seed=0)
+    out, last = run_gpu(inp, dev)
+    rng = np.random.default_rng(123)
+    bs = np.unique(np.concatenate([[0, cfg.batch - 1], rng.integers(0, cfg.batch, 2)]))
+    ds = np.unique(np.concatenate([[0, 1, cfg.dim - 1], rng.integers(0, cfg.dim, 29)]))
+    rout, rlast = sampled_oracle(inp, bs, ds)
+    gout = out[bs][:, :, ds]
+    glast = last[bs][:, ds]
+    e1, e2 = parity_err(gout, rout), parity_err(glast, rlast)
+    assert e1 <= TOL[cfg.dtype] and e2 <= TOL[cfg.dtype], f"{name}: out {e1:.2e} last {e2:.2e}"
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(last))
