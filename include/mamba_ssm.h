@@ -135,6 +135,37 @@ MAMBA_API mamba_status_t mamba_selective_scan_fwd_ex(
     float *last_state, const mamba_scan_plan_t *plan, mamba_stream_t stream);
 
 /*
+ * Allocation-free variant of mamba_selective_scan_fwd_ex. The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory while they run: code inside a custom allocator or a memory-pool
+ * callback, or a runtime that forbids allocation after start-up. The regular
+ * entry point may take a temporary workspace with cudaMallocAsync; this one
+ * never calls cudaMalloc, cudaMallocAsync, cudaFree or any other allocating
+ * routine, and uses instead a static device array of
+ * MAMBA_NOALLOC_SCRATCH_BYTES (16 MiB) that every device loading the library
+ * holds until the process exits. The caller still passes all inputs and
+ * outputs.
+ *   - The split-sequence workspace of the chosen plan, B * (segments - 1) * D *
+ *     (N + 1) * 4 bytes, must fit in the array; larger requests return
+ *     MAMBA_ERR_UNSUPPORTED with the byte counts in the detail string (pass a
+ *     plan with fewer segments, or segments = 1, which needs no scratch).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the previous call's
+ *     contents. Each call writes every scratch value it reads before reading
+ *     it, so nothing needs clearing, but calls whose kernels overlap on the GPU
+ *     (concurrent streams) race on the array: serialise them.
+ * Arguments, results and errors are otherwise those of mamba_selective_scan_fwd_ex.
+ */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (16u << 20)
+MAMBA_API mamba_status_t mamba_selective_scan_fwd_noalloc(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+    const void *u, const void *delta, const float *A_log,
+    const void *B, const void *C, const float *D, const void *z,
+    const float *delta_bias, const float *initial_state, void *out,
+    float *last_state, const mamba_scan_plan_t *plan, mamba_stream_t stream);
+
+/*
  * The plan mamba_selective_scan_fwd_ex would use for these sizes on the
  * current device, assuming 16-byte aligned pointers: writes the chosen knobs
  * to *chosen (use_tma = 1 if the TMA loader would be used, else 2) and the

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "MAMBA_OK", 1: "MAMBA_ERR_INVALID_ARG", 2: "MAMBA_ERR_UNSUPPO
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_selective_state_update", "mamba_status_string",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
-            "mamba_selective_scan_plan")
+            "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +59,9 @@ def library() -> ctypes.CDLL:
             lib.mamba_selective_scan_fwd.restype = i
             lib.mamba_selective_scan_fwd_ex.argtypes = [i, i, i, i, i] + [vp] * 11 + [ctypes.POINTER(ScanPlan), vp]
             lib.mamba_selective_scan_fwd_ex.restype = i
+            lib.mamba_selective_scan_fwd_noalloc.argtypes = [i, i, i, i, i] + [vp] * 11 + [
+                ctypes.POINTER(ScanPlan), vp]
+            lib.mamba_selective_scan_fwd_noalloc.restype = i
             lib.mamba_selective_state_update.argtypes = [i, i, i, i] + [vp] * 10 + [vp]
             lib.mamba_selective_state_update.restype = i
             lib.mamba_status_string.argtypes = [i]

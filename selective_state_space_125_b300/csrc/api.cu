@@ -433,3 +433,139 @@ mamba_status_t mamba_device_status(int* status_out, mamba_stream_t stream_) {
 int mamba_version(void) { return kVersion; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free scan entry point: the split-sequence workspace lives in a
+// static device array instead of a cudaMallocAsync allocation.
+static __device__ __align__(256) float g_noalloc_scratch[MAMBA_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Looks the array's device address up once per device, with that device current.
+mamba_status_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MAMBA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    float* p = nullptr;
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scan scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MAMBA_OK;
+}
+}  // namespace
+
+extern "C" mamba_status_t mamba_selective_scan_fwd_noalloc(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, const void* u, const void* delta,
+    const float* A_log, const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
+    const float* initial_state, void* out, float* last_state, const mamba_scan_plan_t* plan_knobs,
+    mamba_stream_t stream_) {
+  t_detail.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 0 || dim < 0 || seqlen < 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
+  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
+  if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
+  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
+  if (plan_knobs && (plan_knobs->lanes_per_channel < 0 || plan_knobs->segments < 0 || plan_knobs->use_tma < 0 ||
+                     plan_knobs->use_tma > 2))
+    return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
+  if (batch == 0 || dim == 0) return MAMBA_OK;
+  const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
+  const size_t es = dtype == 0 ? 4 : 2;
+  const size_t n_state = (size_t)batch * dim * dstate;
+  if (!A_log) return fail(MAMBA_ERR_INVALID_ARG, "A_log is NULL");
+  if (seqlen == 0) {
+    if (last_state) {
+      cudaError_t e = initial_state
+                          ? cudaMemcpyAsync(last_state, initial_state, n_state * 4, cudaMemcpyDeviceToDevice, stream)
+                          : cudaMemsetAsync(last_state, 0, n_state * 4, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "empty-sequence last_state");
+    }
+    return MAMBA_OK;
+  }
+  if (!u || !delta || !B || !C || !out)
+    return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL (u=%p delta=%p B=%p C=%p out=%p)", u, delta, B, C,
+                out);
+  const size_t nx = (size_t)batch * seqlen * dim * es;
+  const size_t nbc = (size_t)batch * seqlen * dstate * es;
+  const void* inputs[] = {u, delta, z, B, C, A_log, D, delta_bias, initial_state};
+  const size_t sizes[] = {nx, nx, nx, nbc, nbc, (size_t)dim * dstate * 4, (size_t)dim * 4, (size_t)dim * 4,
+                          n_state * 4};
+  for (int i = 0; i < 9; ++i) {
+    if (overlaps(out, nx, inputs[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "out aliases input %d", i);
+    if (overlaps(last_state, n_state * 4, inputs[i], sizes[i]))
+      return fail(MAMBA_ERR_INVALID_ARG, "last_state aliases input %d", i);
+  }
+  if (overlaps(out, nx, last_state, n_state * 4)) return fail(MAMBA_ERR_INVALID_ARG, "out aliases last_state");
+
+  DeviceInfo di;
+  mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  float* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != MAMBA_OK) return st;
+  Plan plan;
+  st = make_plan(dtype, batch, dim, dstate, seqlen, plan_knobs, di.sms, u, delta, z, B, C, &plan);
+  if (st != MAMBA_OK) return st;
+  const size_t rows = (size_t)batch * (plan.nseg - 1) * dim;
+  const size_t need = rows * (dstate + 1) * sizeof(float);
+  if (need > MAMBA_NOALLOC_SCRATCH_BYTES)
+    return fail(MAMBA_ERR_UNSUPPORTED,
+                "the plan (%d segments) needs %zu bytes of scratch; the static scratch holds %u bytes "
+                "(use fewer segments)", plan.nseg, need, MAMBA_NOALLOC_SCRATCH_BYTES);
+
+  ScanMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const uint32_t cb = uint32_t(kScanThreads / plan.lpc);
+  if (plan.tma_x) {
+    if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+    if ((st = encode_3d(&maps.delta, delta, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+    if (z && (st = encode_3d(&maps.z, z, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+  }
+  if (plan.tma_bc) {
+    if ((st = encode_3d(&maps.B, B, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
+    if ((st = encode_3d(&maps.C, C, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
+  }
+  ScanArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.batch = batch;
+  a.dim = dim;
+  a.dstate = dstate;
+  a.seqlen = seqlen;
+  a.nseg = plan.nseg;
+  a.seg_len = plan.seg_len;
+  a.u = u;
+  a.delta = delta;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.A_log = A_log;
+  a.D = D;
+  a.delta_bias = delta_bias;
+  a.h0 = initial_state;
+  a.out = out;
+  a.last_state = last_state;
+  a.tma_x = plan.tma_x;
+  a.tma_bc = plan.tma_bc;
+  a.status = di.status;
+  a.agg_h = scratch;                      // every value is written by the aggregate pass
+  a.agg_dsum = scratch + rows * dstate;   // before the full pass reads it
+  auto launch = [&](ScanMode mode, unsigned nz) {
+    dim3 grid((dim + cb - 1) / cb, batch, nz);
+    return dtype == 0 ? launch_scan_f32(plan.npl, plan.lpc, mode, a, maps, grid, stream)
+                      : launch_scan_bf16(plan.npl, plan.lpc, mode, a, maps, grid, stream);
+  };
+  cudaError_t e = cudaSuccess;
+  if (plan.nseg > 1) e = launch(ScanMode::kAggregate, plan.nseg - 1);
+  if (e == cudaSuccess) e = launch(ScanMode::kFull, plan.nseg);
+  if (e != cudaSuccess) return cuda_fail(e, "scan launch (no-alloc entry point)");
+  return MAMBA_OK;
+}
