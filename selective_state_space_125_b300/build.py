@@ -22,7 +22,7 @@ LIB = os.path.join(PKG, "libmamba_ssm_b300.so")
 SOURCES = ["api.cu", "scan_f32.cu", "scan_bf16.cu", "state_update.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
-FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                 "-I", INCLUDE, "-I", CSRC, "-Xptxas", "-v", "-DMAMBA_BUILDING_LIBRARY"]
 
 

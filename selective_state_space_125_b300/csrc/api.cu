@@ -133,8 +133,10 @@ int npl_for(int N, int lpc) {
   return 0;
 }
 
-// Threads the planner aims to keep resident (12 warps per SM).
-constexpr int kTargetThreadsPerSM = 384;
+// Threads the planner aims to keep resident: 8 warps per SM. Below that the
+// scan is latency-bound; above it, more lanes per channel or more time
+// segments only add overhead (lane-partial sums, the aggregate pass).
+constexpr int kTargetThreadsPerSM = 256;
 
 struct Plan {
   int npl, lpc, nseg, seg_len, chunk;
@@ -173,8 +175,8 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
     const long long threads = channels * lpc;
     nseg = 1;
     if (threads < target) nseg = int((target + threads - 1) / threads);
-    // keep at least 8 chunks per segment, at most 64 segments
-    nseg = std::min({nseg, 64, std::max(1, L / (8 * v.chunk))});
+    // keep at least 16 chunks per segment, at most 64 segments
+    nseg = std::min({nseg, 64, std::max(1, L / (16 * v.chunk))});
   }
   if (nseg < 1) return fail(MAMBA_ERR_INVALID_ARG, "segments=%d must be >= 1", nseg);
   nseg = std::min(nseg, max_seg);

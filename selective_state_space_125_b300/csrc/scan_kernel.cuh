@@ -10,22 +10,27 @@
 //
 // Layout of work:
 //   - a CTA owns kCB = 128 / LPC channels of one batch row and one time
-//     segment; LPC threads share a channel, each holding NPL of its states in
-//     registers (NPL * LPC >= N, the rest padded with zeros);
+//     segment; LPC consecutive lanes of a warp share a channel, each holding
+//     NPL of its states in registers (NPL * LPC >= N, the rest padded with
+//     zeros);
 //   - time is walked in chunks of kChunk steps. Thread 0 stages each chunk's
 //     u / delta / z tiles ([chunk][channels]) and B / C tiles ([chunk][N])
 //     into shared memory with 3-D TMA loads, kScanStages chunks ahead,
-//     completing on one mbarrier per stage (plain loads when the layout does
-//     not meet TMA's 16-byte rules);
-//   - B / C are widened to fp32 once per chunk and shared by every channel of
-//     the CTA; with LPC > 1, dt = softplus(.) and u are also computed once per
-//     (step, channel) into shared memory, and the LPC partial sums of y are
-//     combined in a separate epilogue pass over the chunk;
+//     completing on one mbarrier per stage. When the layout does not meet
+//     TMA's 16-byte rules the CTA fills the same tiles with plain loads;
+//   - per chunk the CTA widens the B / C tiles to fp32 once for all of its
+//     channels (double-buffered) and passes one barrier;
+//   - steps are taken in groups of LPC: lane q of a channel computes dt =
+//     softplus(delta + bias) for step q of the group and the LPC lanes trade
+//     (dt, u) by warp shuffles; after the group's LPC recurrence steps the
+//     lanes' partial readouts are reduce-scattered by shuffles so that lane q
+//     holds the full y of step q, adds D u, applies the SiLU gate and stores
+//     it. With LPC == 1 a thread does all of this for its own channel;
 //   - bf16 inputs use the fast path: a scaled state s = A h, so that one step
-//     is s <- Abar (s + B u) - B u, and y = sum (C / A) s. Every pair of
-//     states goes through packed f32x2 FMUL/FFMA, the exponentials through
-//     MUFU ex2. fp32 inputs use the precise path on the unscaled state with
-//     expm1f, so that (Abar - 1) / A keeps full relative accuracy.
+//     is s <- Abar (s + B u) - B u, and y = sum (C / A) s, all on packed
+//     f32x2 FMUL/FFMA pairs of states, with Abar by MUFU ex2. fp32 inputs use
+//     the precise path on the unscaled state with expm1f, so that
+//     (Abar - 1) / A keeps full relative accuracy.
 //
 // Time segments (the split-L two-pass scheme): with nseg > 1 the aggregate
 // pass (AGG = true) runs segments 0..nseg-2 from h = 0 and writes each
@@ -43,50 +48,132 @@
 
 namespace mamba {
 
+constexpr size_t scan_a128(size_t x) { return (x + 127) & ~size_t(127); }
+
 template <typename Tin, int NPL, int LPC>
 struct ScanGeom {
   static constexpr int kCB = kScanThreads / LPC;  // channels per CTA
   static constexpr int kNP = NPL * LPC;           // padded state count
-  // Steps per pipeline stage: short for one thread per channel (more CTAs per
-  // SM), shorter for large N so that the B / C tiles fit.
-  static constexpr int kChunk = LPC == 1 ? 16 : (kNP >= 256 ? 8 : (kNP >= 128 ? 16 : 32));
   static constexpr int kES = int(sizeof(Tin));
-  static constexpr size_t a128(size_t x) { return (x + 127) & ~size_t(127); }
-  static constexpr size_t kXTile = a128(size_t(kChunk) * kCB * kES);
-  static constexpr size_t kBCTile = a128(size_t(kChunk) * kNP * kES);
+  static constexpr int kChunk = 16;               // steps per pipeline stage (a multiple of LPC)
+  static constexpr size_t kXTile = scan_a128(size_t(kChunk) * kCB * kES);
+  static constexpr size_t kBCTile = scan_a128(size_t(kChunk) * kNP * kES);
   static constexpr size_t kStage = 3 * kXTile + 2 * kBCTile;
-  static constexpr size_t kBC32 = a128(size_t(kChunk) * 2 * kNP * 4);
-  static constexpr size_t kDU = (LPC > 1) ? a128(size_t(kChunk) * kCB * 8) : 0;
-  static constexpr size_t kYP = (LPC > 1) ? a128(size_t(kChunk) * kCB * LPC * 4) : 0;
-  static constexpr size_t kChan = a128(size_t(kCB) * 2 * 4);  // bias, D per channel
+  static constexpr size_t kBC32 = scan_a128(size_t(kChunk) * 2 * kNP * 4);  // [t][B | C][NP] fp32, x2 buffers
+  static constexpr size_t kChan = scan_a128(size_t(kCB) * 2 * 4);           // bias, D per channel
   static constexpr size_t kBar = 128;
-  static constexpr size_t kSmem = kScanStages * kStage + kBC32 + kDU + kYP + kChan + kBar + 128;
+  static constexpr size_t kOffBC32 = kScanStages * kStage;
+  static constexpr size_t kOffChan = kOffBC32 + 2 * kBC32;
+  static constexpr size_t kOffBar = kOffChan + kChan;
+  static constexpr size_t kSmem = kOffBar + kBar + 128;  // + alignment slack of the dynamic base
+  static_assert(kChunk % LPC == 0, "a chunk holds whole step groups");
   static_assert(kSmem <= 227 * 1024, "scan variant exceeds the shared memory of one CTA");
+  static_assert(NPL % 4 == 0, "states per thread come in groups of four (128-bit B / C loads)");
+};
+
+// One step of the fast path for NPL states held as NPL/2 packed pairs:
+// s <- Abar (s + B u) - B u with Abar = 2^(dt * Ak), and (READ) the partial
+// readout sum_j (C_j * Ik_j) s_j. Bt / Ct point at this thread's states.
+template <int NPL, bool READ>
+__device__ __forceinline__ float step_fast(float2 (&s)[NPL / 2], const float2 (&Ak)[NPL / 2],
+                                           const float2 (&Ik)[NPL / 2], float dt, float u, const float* Bt,
+                                           const float* Ct) {
+  const float2 dd = make_float2(dt, dt);
+  const float2 uu = make_float2(u, u);
+  const float2 nu = make_float2(-u, -u);
+  float2 yy[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};  // two chains of the readout sum
+#pragma unroll
+  for (int j = 0; j < NPL / 2; j += 2) {
+    const float4 B4 = *reinterpret_cast<const float4*>(Bt + 2 * j);
+    float4 C4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (READ) C4 = *reinterpret_cast<const float4*>(Ct + 2 * j);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float2 Bp = h == 0 ? make_float2(B4.x, B4.y) : make_float2(B4.z, B4.w);
+      const float2 x = __fmul2_rn(dd, Ak[j + h]);
+      const float2 ab = make_float2(hw_ex2(x.x), hw_ex2(x.y));
+      const float2 w = __ffma2_rn(Bp, uu, s[j + h]);
+      const float2 nv = __fmul2_rn(Bp, nu);
+      s[j + h] = __ffma2_rn(ab, w, nv);
+      if (READ) {
+        const float2 Cp = h == 0 ? make_float2(C4.x, C4.y) : make_float2(C4.z, C4.w);
+        yy[h] = __ffma2_rn(__fmul2_rn(Cp, Ik[j + h]), s[j + h], yy[h]);
+      }
+    }
+  }
+  return (yy[0].x + yy[1].x) + (yy[0].y + yy[1].y);
+}
+
+// One step of the precise path (unscaled state, expm1f): h <- h + (Abar - 1) h
+// + (Abar - 1) / A * B u, readout sum_j C_j h_j. Ak holds A, Ik holds 1 / A.
+template <int NPL, bool READ>
+__device__ __forceinline__ float step_precise(float2 (&h)[NPL / 2], const float2 (&Ak)[NPL / 2],
+                                              const float2 (&Ik)[NPL / 2], float dt, float u, const float* Bt,
+                                              const float* Ct) {
+  float y = 0.0f;
+#pragma unroll
+  for (int j = 0; j < NPL / 2; ++j) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float A = k == 0 ? Ak[j].x : Ak[j].y;
+      const float I = k == 0 ? Ik[j].x : Ik[j].y;
+      float& hv = k == 0 ? h[j].x : h[j].y;
+      const float x = dt * A;
+      const float e = expm1f(x);                     // Abar - 1
+      const float coef = (x != 0.0f) ? e * I : dt;   // (Abar - 1) / A, limit dt
+      hv = fmaf(coef * Bt[2 * j + k], u, fmaf(e, hv, hv));
+      if (READ) y = fmaf(Ct[2 * j + k], hv, y);
+    }
+  }
+  return y;
+}
+
+// Sum over the LPC lanes of a channel of v[0..LPC), scattered so that lane q
+// returns the total of entry q (recursive halving over xor partners).
+template <int LPC>
+__device__ __forceinline__ float reduce_scatter(float (&v)[LPC], int q) {
+#pragma unroll
+  for (int m = LPC / 2; m >= 1; m /= 2) {
+    const bool hi = (q & m) != 0;
+#pragma unroll
+    for (int i = 0; i < m; ++i) {
+      const float send = hi ? v[i] : v[i + m];
+      const float keep = hi ? v[i + m] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+  }
+  return v[0];
+}
+
+// CTAs per SM each variant's register budget is sized for: 8 (<= 64
+// registers) with 4 states per thread, 7 (<= 72) with 8, 4 (<= 128) with 16.
+template <int NPL>
+struct ScanMinBlocks {
+  static constexpr int value = NPL <= 4 ? 8 : (NPL <= 8 ? 7 : 4);
 };
 
 template <typename Tin, int NPL, int LPC, bool AGG>
-__global__ void __launch_bounds__(kScanThreads)
+__global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     scan_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   using G = ScanGeom<Tin, NPL, LPC>;
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
   constexpr int CB = G::kCB, NP = G::kNP, CH = G::kChunk;
-  static_assert(NPL % 2 == 0, "states per thread come in pairs");
+  constexpr int NH = NPL / 2;
 
   extern __shared__ unsigned char smem_dyn[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
-  float* bc32 = reinterpret_cast<float*>(smem + kScanStages * G::kStage);
-  float2* du = reinterpret_cast<float2*>(smem + kScanStages * G::kStage + G::kBC32);
-  float* yp = reinterpret_cast<float*>(smem + kScanStages * G::kStage + G::kBC32 + G::kDU);
-  float* chan_bias = reinterpret_cast<float*>(smem + kScanStages * G::kStage + G::kBC32 + G::kDU + G::kYP);
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
+  float* chan_bias = reinterpret_cast<float*>(smem + G::kOffChan);
   float* chan_D = chan_bias + CB;
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + kScanStages * G::kStage + G::kBC32 + G::kDU + G::kYP + G::kChan);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + G::kOffBar);
 
   auto xu = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage); };
   auto xd = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kXTile); };
   auto xz = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 2 * G::kXTile); };
   auto braw = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 3 * G::kXTile); };
   auto craw = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 3 * G::kXTile + G::kBCTile); };
+  auto bc32 = [&](int k) { return reinterpret_cast<float*>(smem + G::kOffBC32 + (k & 1) * G::kBC32); };
 
   const int tid = threadIdx.x;
   const int c = tid / LPC, q = tid % LPC;
@@ -114,35 +201,8 @@ __global__ void __launch_bounds__(kScanThreads)
     chan_D[i] = (a.D && dd < Dm) ? a.D[dd] : 0.0f;
   }
 
-  // Per-thread constants: A_n = -exp(A_log) for my NPL states.
-  //  fast:    Ak[j] = A * log2(e) (exponent for ex2), Ik[j] = 1 / A;
-  //  precise: Ak[j] = A,                              Ik[j] = 1 / A (0 if A == 0).
-  float Ak[NPL], Ik[NPL], h[NPL];
-#pragma unroll
-  for (int j = 0; j < NPL; ++j) {
-    const int n = q * NPL + j;
-    float A = -1.0f;
-    if (dvalid && n < N) A = -expf(a.A_log[(size_t)d * N + n]);
-    if (!PRECISE) A = fminf(A, -1e-30f);
-    const bool real = n < N;
-    Ak[j] = real ? (PRECISE ? A : A * kLog2e) : 0.0f;
-    Ik[j] = (real && A != 0.0f) ? 1.0f / A : 0.0f;
-    // Initial state: h0 (or 0), then the composed aggregates of earlier segments.
-    float hin = 0.0f;
-    if (!AGG && real && dvalid) {
-      if (a.h0) hin = a.h0[((size_t)b * Dm + d) * N + n];
-      for (int k = 0; k < seg; ++k) {
-        const size_t row = (size_t)b * (a.nseg - 1) + k;
-        const float ds = a.agg_dsum[row * Dm + d];
-        const float decay = PRECISE ? expf(A * ds) : hw_ex2(Ak[j] * ds);
-        hin = fmaf(decay, hin, a.agg_h[(row * Dm + d) * N + n]);
-      }
-    }
-    h[j] = PRECISE ? hin : hin * A;  // fast path keeps s = A h
-  }
-
-  // Chunk staging.
-  auto issue = [&](int k) {  // thread 0 only
+  // Chunk staging by TMA (thread 0 only).
+  auto issue = [&](int k) {
     const int s = k % kScanStages;
     const int t0 = t_begin + k * CH;
     uint32_t bytes = 0;
@@ -174,11 +234,110 @@ __global__ void __launch_bounds__(kScanThreads)
     }
   }
   __syncthreads();
+  int issued = 0;  // chunks handed to TMA so far (thread 0)
   if (use_tma && tid == 0)
-    for (int k = 0; k < min(kScanStages, nchunks); ++k) issue(k);
+    for (; issued < min(kScanStages, nchunks); ++issued) issue(issued);
 
-  float dsum = 0.0f;   // AGG: sum of dt over the segment (fast path)
+  // Per-thread constants for my NPL states:
+  //  fast:    Ak = A * log2(e) (exponent for ex2), Ik = 1 / A;
+  //  precise: Ak = A,                              Ik = 1 / A (0 if A == 0).
+  // Initial state: h0 (or 0), then the composed aggregates of earlier segments.
+  float2 Ak[NH], Ik[NH], st[NH];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int n = q * NPL + j;
+    const bool real = n < N;
+    float A = -1.0f;
+    if (dvalid && real) A = -expf(a.A_log[(size_t)d * N + n]);
+    if (!PRECISE) A = fminf(A, -1e-30f);
+    const float ak = real ? (PRECISE ? A : A * kLog2e) : 0.0f;
+    const float ik = (real && A != 0.0f) ? 1.0f / A : 0.0f;
+    float hin = 0.0f;
+    if (!AGG && real && dvalid) {
+      if (a.h0) hin = a.h0[((size_t)b * Dm + d) * N + n];
+      for (int k = 0; k < seg; ++k) {
+        const size_t row = (size_t)b * (a.nseg - 1) + k;
+        const float ds = a.agg_dsum[row * Dm + d];
+        const float decay = PRECISE ? expf(A * ds) : hw_ex2(ak * ds);
+        hin = fmaf(decay, hin, a.agg_h[(row * Dm + d) * N + n]);
+      }
+    }
+    const float sv = PRECISE ? hin : hin * A;  // fast path keeps s = A h
+    if (j % 2 == 0) {
+      Ak[j / 2].x = ak;
+      Ik[j / 2].x = ik;
+      st[j / 2].x = sv;
+    } else {
+      Ak[j / 2].y = ak;
+      Ik[j / 2].y = ik;
+      st[j / 2].y = sv;
+    }
+  }
+  const float bias = chan_bias[c];
+  const float Dd = chan_D[c];
+
+  float dsum = 0.0f;    // AGG: sum of dt over the segment (fast path)
   double dsum_d = 0.0;  // AGG: the same in fp64 (precise path)
+
+  // The steps of one staged chunk (see the loop below).
+  auto run_chunk = [&]<bool HZ>(int s, int kc, int t0, int tv) {
+    const Tin* su = xu(s) + c;
+    const Tin* sd = xd(s) + c;
+    const Tin* sz = xz(s) + c;
+    const float* bcq = bc32(kc) + q * NPL;
+    Tin* gout = static_cast<Tin*>(a.out) + ((size_t)b * L + t0 + q) * Dm + d;
+    (void)gout;
+    // dt and u of step q of the first group, computed by this lane
+    auto lane_dtu = [&](int tm, float& dtv, float& uv) {
+      const float um = E::load(su + tm * CB);
+      const float xm = E::load(sd + tm * CB) + bias;
+      const float dt = PRECISE ? softplus_precise(xm) : softplus_fast(xm);
+      const bool live = tm < tv;
+      dtv = live ? dt : 0.0f;
+      uv = live ? um : 0.0f;
+    };
+    float dt_nx, u_nx;
+    lane_dtu(q, dt_nx, u_nx);
+    [[maybe_unused]] float y_pv = 0.0f, u_pv = 0.0f, z_pv = 0.0f;  // previous group's readout, pending its epilogue
+#pragma unroll 4
+    for (int tg = 0; tg < CH; tg += LPC) {
+      const float dt_cu = dt_nx, u_cu = u_nx;
+      float z_cu = 0.0f;
+      if (!AGG && HZ) z_cu = E::load(sz + (tg + q) * CB);
+      if (tg + LPC < CH) lane_dtu(tg + LPC + q, dt_nx, u_nx);
+      float yp[LPC];
+#pragma unroll
+      for (int j = 0; j < LPC; ++j) {
+        const int src = (tid & 31) - q + j;
+        const float dt = LPC == 1 ? dt_cu : __shfl_sync(0xffffffffu, dt_cu, src);
+        const float u = LPC == 1 ? u_cu : __shfl_sync(0xffffffffu, u_cu, src);
+        const float* Bt = bcq + (tg + j) * 2 * NP;
+        if constexpr (PRECISE)
+          yp[j] = step_precise<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
+        else
+          yp[j] = step_fast<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
+        if constexpr (AGG) {
+          if (PRECISE) dsum_d += dt; else dsum += dt;
+        }
+      }
+      if constexpr (!AGG) {
+        // epilogue of the previous group: D skip, gate, store
+        if (tg > 0) {
+          float y = fmaf(Dd, u_pv, y_pv);
+          if (HZ) y *= PRECISE ? silu_precise(z_pv) : silu_fast(z_pv);
+          if (dvalid && tg - LPC + q < tv) E::store(gout + (size_t)(tg - LPC) * Dm, y);
+        }
+        y_pv = reduce_scatter<LPC>(yp, q);  // full readout of step tg + q
+        u_pv = u_cu;
+        z_pv = z_cu;
+      }
+    }
+    if constexpr (!AGG) {
+      float y = fmaf(Dd, u_pv, y_pv);
+      if (HZ) y *= PRECISE ? silu_precise(z_pv) : silu_fast(z_pv);
+      if (dvalid && CH - LPC + q < tv) E::store(gout + (size_t)(CH - LPC) * Dm, y);
+    }
+  };
 
   for (int k = 0; k < nchunks; ++k) {
     const int s = k % kScanStages;
@@ -191,145 +350,58 @@ __global__ void __launch_bounds__(kScanThreads)
         if (tid == 0) {
           record_status(a.status, kStatusTimeout);
           // Let copies already in flight land before the CTA's shared memory goes away.
-          for (int kk = k; kk < min(k + kScanStages, nchunks); ++kk)
-            mbar_wait_bounded(&mbar[kk % kScanStages], (kk / kScanStages) & 1);
+          for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&mbar[kk % kScanStages], (kk / kScanStages) & 1);
         }
         return;
       }
     }
-    if (!a.tma_x || !a.tma_bc) {
-      // Plain loads (layouts TMA cannot describe); zero outside the tensor.
-      if (!a.tma_x) {
-        for (int i = tid; i < CH * CB; i += kScanThreads) {
-          const int t = i / CB, cc = i % CB;
-          const int gt = t0 + t, gd = d0 + cc;
-          const bool in = gt < L && gd < Dm;
-          const size_t off = ((size_t)b * L + gt) * Dm + gd;
-          xu(s)[i] = in ? gu[off] : Tin(0.0f);
-          xd(s)[i] = in ? gdl[off] : Tin(0.0f);
-          if (has_z) xz(s)[i] = in ? gz[off] : Tin(0.0f);
-        }
-      }
-      if (!a.tma_bc) {
-        for (int i = tid; i < CH * NP; i += kScanThreads) {
-          const int t = i / NP, n = i % NP;
-          const int gt = t0 + t;
-          const bool in = gt < L && n < N;
-          const size_t off = ((size_t)b * L + gt) * N + n;
-          bc32[t * 2 * NP + n] = in ? E::load(gB + off) : 0.0f;
-          bc32[t * 2 * NP + NP + n] = in ? E::load(gC + off) : 0.0f;
-        }
-      }
-      __syncthreads();
-    }
-    if (a.tma_bc) {
-      for (int i = tid; i < CH * NP; i += kScanThreads) {
-        const int t = i / NP, n = i % NP;
-        const bool in = n < N;
-        bc32[t * 2 * NP + n] = in ? E::load(braw(s) + t * N + n) : 0.0f;
-        bc32[t * 2 * NP + NP + n] = in ? E::load(craw(s) + t * N + n) : 0.0f;
-      }
-    }
-    if constexpr (LPC > 1) {
+    // Plain loads into the tiles where TMA cannot be used (zero outside the tensor).
+    if (!a.tma_x) {
       for (int i = tid; i < CH * CB; i += kScanThreads) {
-        const int cc = i % CB;
-        const float x = E::load(xd(s) + i) + chan_bias[cc];
-        du[i] = make_float2(PRECISE ? softplus_precise(x) : softplus_fast(x), E::load(xu(s) + i));
-      }
-    }
-    __syncthreads();
-
-    // ---- the recurrence over this chunk
-    const Tin* su = xu(s);
-    const Tin* sd = xd(s);
-    const Tin* sz = xz(s);
-    const float bias = chan_bias[c];
-    const float Dd = chan_D[c];
-    for (int t = 0; t < tv; ++t) {
-      float dt, uf;
-      if constexpr (LPC == 1) {
-        uf = E::load(su + t * CB + c);
-        const float x = E::load(sd + t * CB + c) + bias;
-        dt = PRECISE ? softplus_precise(x) : softplus_fast(x);
-      } else {
-        const float2 v = du[t * CB + c];
-        dt = v.x;
-        uf = v.y;
-      }
-      const float* Bt = bc32 + t * 2 * NP + q * NPL;
-      const float* Ct = Bt + NP;
-      float y;
-      if constexpr (PRECISE) {
-        y = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NPL; ++j) {
-          const float x = dt * Ak[j];
-          const float e = expm1f(x);                 // Abar - 1
-          const float coef = (x != 0.0f) ? e * Ik[j] : dt;  // (Abar - 1) / A, limit dt
-          h[j] = fmaf(coef * Bt[j], uf, fmaf(e, h[j], h[j]));
-          if (!AGG) y = fmaf(Ct[j], h[j], y);
-        }
-      } else {
-        const float2 dd = make_float2(dt, dt);
-        const float2 uu = make_float2(uf, uf);
-        const float2 nu = make_float2(-uf, -uf);
-        float2 yy = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int j = 0; j < NPL; j += 2) {
-          const float2 x = __fmul2_rn(dd, make_float2(Ak[j], Ak[j + 1]));
-          const float2 ab = make_float2(hw_ex2(x.x), hw_ex2(x.y));
-          const float2 Bp = *reinterpret_cast<const float2*>(Bt + j);
-          const float2 w = __ffma2_rn(Bp, uu, make_float2(h[j], h[j + 1]));
-          const float2 nv = __fmul2_rn(Bp, nu);
-          const float2 sn = __ffma2_rn(ab, w, nv);
-          h[j] = sn.x;
-          h[j + 1] = sn.y;
-          if (!AGG) {
-            const float2 Cp = *reinterpret_cast<const float2*>(Ct + j);
-            const float2 ci = __fmul2_rn(Cp, make_float2(Ik[j], Ik[j + 1]));
-            yy = __ffma2_rn(ci, sn, yy);
-          }
-        }
-        y = yy.x + yy.y;
-      }
-      if constexpr (AGG) {
-        if (PRECISE) dsum_d += dt; else dsum += dt;
-      } else if constexpr (LPC == 1) {
-        if (dvalid) {
-          y = fmaf(Dd, uf, y);
-          if (has_z) {
-            const float zf = E::load(sz + t * CB + c);
-            y *= PRECISE ? silu_precise(zf) : silu_fast(zf);
-          }
-          E::store(static_cast<Tin*>(a.out) + ((size_t)b * L + t0 + t) * Dm + d, y);
-        }
-      } else {
-        yp[(t * CB + c) * LPC + q] = y;
-      }
-    }
-
-    if constexpr (!AGG && LPC > 1) {
-      __syncthreads();
-      for (int i = tid; i < tv * CB; i += kScanThreads) {
         const int t = i / CB, cc = i % CB;
-        const int gd = d0 + cc;
-        if (gd >= Dm) continue;
-        float y = 0.0f;
-#pragma unroll
-        for (int r = 0; r < LPC; ++r) y += yp[i * LPC + r];
-        y = fmaf(chan_D[cc], du[i].y, y);
-        if (has_z) {
-          const float zf = E::load(sz + i);
-          y *= PRECISE ? silu_precise(zf) : silu_fast(zf);
-        }
-        E::store(static_cast<Tin*>(a.out) + ((size_t)b * L + t0 + t) * Dm + gd, y);
+        const int gt = t0 + t, gd = d0 + cc;
+        const bool in = gt < L && gd < Dm;
+        const size_t off = ((size_t)b * L + gt) * Dm + gd;
+        xu(s)[i] = in ? gu[off] : Tin(0.0f);
+        xd(s)[i] = in ? gdl[off] : Tin(0.0f);
+        if (has_z) xz(s)[i] = in ? gz[off] : Tin(0.0f);
       }
     }
-    __syncthreads();  // every read of stage s, bc32, du and yp is done
-    if (use_tma && tid == 0 && k + kScanStages < nchunks) {
-      fence_proxy_async_smem();
-      issue(k + kScanStages);
+    // B / C rows widened to fp32 once for every channel of the CTA (zero beyond N).
+    float* bck = bc32(k);
+    for (int i = tid; i < CH * NP; i += kScanThreads) {
+      const int t = i / NP, n = i % NP;
+      float bv = 0.0f, cv = 0.0f;
+      if (n < N) {
+        if (a.tma_bc) {
+          bv = E::load(braw(s) + t * N + n);
+          cv = E::load(craw(s) + t * N + n);
+        } else if (t0 + t < L) {
+          const size_t off = ((size_t)b * L + t0 + t) * N + n;
+          bv = E::load(gB + off);
+          cv = E::load(gC + off);
+        }
+      }
+      bck[t * 2 * NP + n] = bv;
+      bck[t * 2 * NP + NP + n] = cv;
     }
+    __syncthreads();  // chunk k staged; every thread is past chunk k-1
+    if (use_tma && tid == 0 && k >= 1 && issued < nchunks) {
+      fence_proxy_async_smem();  // chunk k-1's stage was read through the generic proxy
+      issue(issued);
+      ++issued;
+    }
+
+    // ---- the recurrence over chunk k, in groups of LPC steps. Every chunk
+    // runs all CH steps: steps at or past tv (the end of the sequence or of
+    // the segment) get dt = 0 and u = 0, which leaves the state exactly as it
+    // is (Abar = 1, no input), and store nothing. The loop is branch-free and
+    // fully unrolled so that the compiler can overlap a group's recurrence
+    // with the next group's softplus and the previous group's epilogue.
+    if (has_z)
+      run_chunk.template operator()<true>(s, k, t0, tv);
+    else
+      run_chunk.template operator()<false>(s, k, t0, tv);
   }
 
   if (!dvalid) return;
@@ -338,7 +410,9 @@ __global__ void __launch_bounds__(kScanThreads)
 #pragma unroll
     for (int j = 0; j < NPL; ++j) {
       const int n = q * NPL + j;
-      if (n < N) a.agg_h[(row * Dm + d) * N + n] = PRECISE ? h[j] : h[j] * Ik[j];
+      const float sv = (j % 2 == 0) ? st[j / 2].x : st[j / 2].y;
+      const float ik = (j % 2 == 0) ? Ik[j / 2].x : Ik[j / 2].y;
+      if (n < N) a.agg_h[(row * Dm + d) * N + n] = PRECISE ? sv : sv * ik;
     }
     if (q == 0) a.agg_dsum[row * Dm + d] = PRECISE ? float(dsum_d) : dsum;
   } else {
@@ -346,7 +420,9 @@ __global__ void __launch_bounds__(kScanThreads)
 #pragma unroll
       for (int j = 0; j < NPL; ++j) {
         const int n = q * NPL + j;
-        if (n < N) a.last_state[((size_t)b * Dm + d) * N + n] = PRECISE ? h[j] : h[j] * Ik[j];
+        const float sv = (j % 2 == 0) ? st[j / 2].x : st[j / 2].y;
+        const float ik = (j % 2 == 0) ? Ik[j / 2].x : Ik[j / 2].y;
+        if (n < N) a.last_state[((size_t)b * Dm + d) * N + n] = PRECISE ? sv : sv * ik;
       }
     }
   }

@@ -72,8 +72,8 @@ def test_no_alloc_matches_regular_entry_point_twice(dev, dtype):
 def test_no_alloc_refuses_a_workspace_larger_than_its_array(dev):
     import torch
     from selective_state_space_125_b300 import binding
-    # N = 256, 3 segments: 4 * 2 * 2048 * 257 * 4 bytes = 16.8 MB > 16 MiB
-    inp = make_scan_inputs(4, 2048, 256, 24, "bf16", seed=3)
+    # N = 256, 3 segments of 16 steps: 4 * 2 * 2048 * 257 * 4 bytes = 16.8 MB > 16 MiB
+    inp = make_scan_inputs(4, 2048, 256, 48, "bf16", seed=3)
     t = upload_scan(inp, dev)
     out = torch.empty_like(t["u"])
     last = torch.empty((4, 2048, 256), dtype=torch.float32, device=dev)
