@@ -33,8 +33,12 @@ from selective_state_space_125_b300.workloads import (SCAN_CONFIGS, bf16_bits,  
 
 METRIC = "selective-scan channel-steps/s"
 L2_BYTES = 126 * 2**20
-FP32_LANES_PER_SM = 128          # FP32 lane-ops per clock per SM (B300)
-ALG_OPS_PER_STATE_STEP = 6       # FP32 ops per (channel, step, state) of the scan, see the design doc
+FP32_LANES_PER_SM = 128          # FP32 lanes per SM (B300): one FMUL/FADD/FFMA lane-op each per clock
+# FP32 lane-ops per (channel, step, state) that the bf16 scan needs: dt*A,
+# the input product, the two FMAs of the state update and the two of the
+# readout (C / A times the scaled state, accumulated); exp runs on MUFU.
+ALG_OPS_PER_STATE_STEP = 6
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_traffic.json")
 
 
 def parse():
@@ -50,6 +54,7 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
     p.add_argument("--lanes", type=int, default=0, help="plan override: lanes per channel")
     p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
+    p.add_argument("--no-decode", action="store_true", help="skip the full-size decode measurement")
     return p.parse_args()
 
 
@@ -119,6 +124,74 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(inside)}
+
+
+def kernel_source_sha():
+    """Hash of the CUDA sources, so that stored ncu figures are used only for the kernel they measured."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_125_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measure_decode(device, stream, peaks, calls=200):
+    """Decode step on the full decode workloads (B128 D5120, N = 16 and 128): us per call and GB/s.
+
+    Each call reads and writes the resident fp32 state and reads one token's
+    bf16 activations; 16 distinct tokens are cycled. Calls rotate over enough
+    independent state buffers (one per layer of a model, say) that together
+    exceed three times L2, so every call streams its state from HBM."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    from selective_state_space_125_b300.workloads import DECODE_CONFIGS, make_decode_config_inputs
+    out = {}
+    for name in ("decode", "decode128"):
+        cfg = DECODE_CONFIGS[name]
+        inp = make_decode_config_inputs(cfg, seed=0)
+        B, Dm, N = cfg.batch, cfg.dim, cfg.dstate
+        bf = lambda a: torch.from_numpy(bf16_bits(a).view(np.int16)).to(device).view(torch.bfloat16)
+        f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+        state0 = f32(inp["state0"])
+        nbuf = max(1, int(np.ceil(3 * L2_BYTES / (state0.numel() * 4))))
+        states = [state0] + [state0.clone() for _ in range(nbuf - 1)]
+        toks = [{k: bf(inp[k][p]) for k in ("u", "delta", "z", "B", "C")} for p in range(cfg.pool)]
+        A_log, Dv, bias = f32(inp["A_log"]), f32(inp["D"]), f32(inp["delta_bias"])
+        y = torch.empty((B, Dm), dtype=torch.bfloat16, device=device)
+
+        # Raw C-ABI calls with the pointers marshalled once: a call then costs the host
+        # about a microsecond, well under the kernel's time, so launches stay queued.
+        lib = binding.library()
+        sh = stream.cuda_stream
+        argv = [[(B, Dm, N, binding.MAMBA_BF16, st.data_ptr(), t["u"].data_ptr(), t["delta"].data_ptr(),
+                  A_log.data_ptr(), t["B"].data_ptr(), t["C"].data_ptr(), Dv.data_ptr(), t["z"].data_ptr(),
+                  bias.data_ptr(), y.data_ptr(), sh) for t in toks] for st in states]
+        binding.mamba_selective_state_update(state0, toks[0]["u"], toks[0]["delta"], A_log, toks[0]["B"],
+                                             toks[0]["C"], Dv, toks[0]["z"], bias, y)  # checked once
+
+        def call(i):
+            if lib.mamba_selective_state_update(*argv[i % nbuf][(i // nbuf) % cfg.pool]) != 0:
+                raise RuntimeError("decode step failed")
+        for i in range(10):
+            call(i)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(calls):
+            call(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        us = e0.elapsed_time(e1) / calls * 1e3
+        alg = B * Dm * N * 4 * 2 + 4 * B * Dm * 2 + 2 * B * N * 2 + Dm * N * 4 + 2 * Dm * 4
+        gbs = alg / (us * 1e-6) / 1e9
+        out[name] = {"workload": cfg.description, "us_per_call": us, "channel_steps_per_s": B * Dm / (us * 1e-6),
+                     "bytes_per_call": alg, "GB/s": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "calls": calls,
+                     "state_buffers": nbuf}
+        del states, state0, toks
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------- our arm
@@ -244,17 +317,20 @@ def run_ours(args, rank, world, device):
     alg_bytes = (4 * es * B * L * Dm + 2 * N * es * B * L + Dm * N * 4 + 2 * Dm * 4
                  + (B * Dm * N * 4 if cfg.last_state else 0))
     alg_ops = ALG_OPS_PER_STATE_STEP * N * B * L * Dm
-    achieved_gops = alg_ops / (scan_avg_ms / 1e3) / 1e9
-    peak_gops = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e9
+    achieved_tops = alg_ops / (scan_avg_ms / 1e3) / 1e12
+    peak_tops = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e12
     achieved_gbs = alg_bytes / (scan_avg_ms / 1e3) / 1e9
     clocks = sampler.summary(t_wall0, t_wall1)
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "scan_traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
+    traffic, traffic_note = None, "no ncu summary for this workload and plan"
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
             tr = json.load(f).get(args.workload)
-        if tr and tr.get("plan") == [chosen.lanes_per_channel, chosen.segments]:
-            traffic = tr.get("dram_bytes_per_launch")
+        if tr and tr.get("plan") == [chosen.lanes_per_channel, chosen.segments] and \
+                tr.get("kernel_source_sha") == kernel_source_sha():
+            traffic, traffic_note = tr.get("dram_bytes_per_call"), tr.get("source")
+        elif tr:
+            traffic_note = "ncu summary is for another plan or an older kernel"
+    decode = None if args.no_decode else measure_decode(device, stream, peaks)
     result = {
         "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -264,11 +340,12 @@ def run_ours(args, rank, world, device):
                    "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB (> L2)",
                    "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
                             "tma": chosen.use_tma == 1}},
-        "roofline": {"bound": "alu", "achieved": achieved_gops, "peak": peak_gops, "unit": "Gop/s",
-                     "frac": achieved_gops / peak_gops, "traffic": traffic,
-                     "kernel": "selective scan call (all passes)", "kernel_ms": scan_avg_ms,
+        "roofline": {"bound": "alu", "achieved": achieved_tops, "peak": peak_tops, "unit": "T FP32 lane-op/s",
+                     "frac": achieved_tops / peak_tops, "traffic": traffic, "traffic_source": traffic_note,
+                     "kernel": f"selective scan call ({scan_launches} launch(es))", "kernel_ms": scan_avg_ms,
                      "ops_per_launch": alg_ops,
-                     "peak_basis": f"{FP32_LANES_PER_SM} FP32 lanes x {sms} SMs x {peaks['sm_max_mhz']:.0f} MHz"},
+                     "peak_basis": f"{FP32_LANES_PER_SM} FP32 lanes x {sms} SMs x {peaks['sm_max_mhz']:.0f} MHz "
+                                   "(recipe unit counts and maximum SM clock)"},
         "hbm": {"achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"], "bytes_per_launch": alg_bytes,
                 "peak_source": f"MEASURED_PEAKS.json ({peaks['source']})"},
@@ -277,6 +354,8 @@ def run_ours(args, rank, world, device):
         "gpu_launches": K * (scan_launches + 1),
         "clocks": clocks,
     }
+    if decode is not None:
+        result["decode"] = decode
     return result
 
 

@@ -133,10 +133,21 @@ int npl_for(int N, int lpc) {
   return 0;
 }
 
-// Threads the planner aims to keep resident: 8 warps per SM. Below that the
-// scan is latency-bound; above it, more lanes per channel or more time
-// segments only add overhead (lane-partial sums, the aggregate pass).
+// Plan choice, from sweeps of the scan on B300 (bf16, N = 16):
+//  - with at least 8 resident warps per SM of channels (B * D >= 256 per SM),
+//    one lane per channel and no time split is fastest: the fewest
+//    instructions per state and no aggregate pass;
+//  - long sequences (L >= kLongSeq) with fewer channels split time into
+//    segments of at least kMinSegSteps steps, one lane per channel, aiming at
+//    32 warps per SM: the aggregate pass costs about 0.6 of a full pass over
+//    the same steps, less than the lane-sharing overhead and the idle SMs it
+//    replaces;
+//  - otherwise the states of a channel are spread over up to 4 lanes to
+//    reach 8 warps per SM, then time is split if that is still short.
 constexpr int kTargetThreadsPerSM = 256;
+constexpr int kLongTargetThreadsPerSM = 1024;
+constexpr int kLongSeq = 8192;
+constexpr int kMinSegSteps = 512;
 
 struct Plan {
   int npl, lpc, nseg, seg_len, chunk;
@@ -150,16 +161,20 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
   int lpc_min = 1;
   while (lpc_min * 16 < N) lpc_min *= 2;
   int lpc = knobs ? knobs->lanes_per_channel : 0;
+  int nseg = knobs ? knobs->segments : 0;
   const long long channels = (long long)batch * dim;
   const long long target = (long long)sms * kTargetThreadsPerSM;
+  const bool long_split = channels * lpc_min < target && L >= kLongSeq;
   if (lpc == 0) {
-    // Spread a channel's states over more threads while that is needed to
-    // fill the device, as long as each thread keeps at least 4 real states.
     lpc = lpc_min;
-    ScanVariant probe;
-    while (channels * lpc < target && lpc * 2 <= 16 && N >= 4 * lpc * 2 &&
-           variant_for(dtype, npl_for(N, lpc * 2), lpc * 2, &probe))
-      lpc *= 2;
+    if (!long_split) {
+      // Spread a channel's states over more threads while that is needed to
+      // fill the device, up to 4 lanes and at least 4 real states per lane.
+      ScanVariant probe;
+      while (channels * lpc < target && lpc * 2 <= std::max(4, lpc_min) && N >= 4 * lpc * 2 &&
+             variant_for(dtype, npl_for(N, lpc * 2), lpc * 2, &probe))
+        lpc *= 2;
+    }
   }
   if (lpc < lpc_min || (lpc & (lpc - 1)) != 0 || lpc > 16)
     return fail(MAMBA_ERR_INVALID_ARG, "lanes_per_channel=%d is not a power of two in [%d, 16] for N=%d", lpc,
@@ -169,14 +184,14 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
   if (npl == 0 || !variant_for(dtype, npl, lpc, &v))
     return fail(MAMBA_ERR_UNSUPPORTED, "no scan kernel for N=%d with lanes_per_channel=%d", N, lpc);
 
-  int nseg = knobs ? knobs->segments : 0;
   const int max_seg = std::max(1, std::min(65535, (L + v.chunk - 1) / v.chunk));
   if (nseg == 0) {
     const long long threads = channels * lpc;
+    const long long want = long_split ? (long long)sms * kLongTargetThreadsPerSM : target;
     nseg = 1;
-    if (threads < target) nseg = int((target + threads - 1) / threads);
-    // keep at least 16 chunks per segment, at most 64 segments
-    nseg = std::min({nseg, 64, std::max(1, L / (16 * v.chunk))});
+    if (threads < want) nseg = int((want + threads - 1) / threads);
+    // segments of at least kMinSegSteps steps, at most 64 segments
+    nseg = std::min({nseg, 64, std::max(1, L / kMinSegSteps)});
   }
   if (nseg < 1) return fail(MAMBA_ERR_INVALID_ARG, "segments=%d must be >= 1", nseg);
   nseg = std::min(nseg, max_seg);
@@ -370,6 +385,7 @@ mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamb
   if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
   if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
     return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  if (batch > 4 * 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds %d", batch, 4 * 65535);
   if (batch == 0 || dim == 0) return MAMBA_OK;
   if (!state || !u || !delta || !A_log || !B || !C || !out)
     return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL");

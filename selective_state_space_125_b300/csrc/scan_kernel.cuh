@@ -129,19 +129,26 @@ __device__ __forceinline__ float step_precise(float2 (&h)[NPL / 2], const float2
 }
 
 // Sum over the LPC lanes of a channel of v[0..LPC), scattered so that lane q
-// returns the total of entry q (recursive halving over xor partners).
+// returns the total of entry q: recursive halving over xor partners, one
+// round per bit of q from the highest (M = LPC / 2) down to 1. Written as a
+// compile-time recursion so that every index into v is static.
+template <int M, int LPC>
+__device__ __forceinline__ void reduce_scatter_round(float (&v)[LPC], int q) {
+  if constexpr (M >= 1) {
+    const bool hi = (q & M) != 0;
+#pragma unroll
+    for (int i = 0; i < M; ++i) {
+      const float send = hi ? v[i] : v[i + M];
+      const float keep = hi ? v[i + M] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+    }
+    reduce_scatter_round<M / 2, LPC>(v, q);
+  }
+}
+
 template <int LPC>
 __device__ __forceinline__ float reduce_scatter(float (&v)[LPC], int q) {
-#pragma unroll
-  for (int m = LPC / 2; m >= 1; m /= 2) {
-    const bool hi = (q & m) != 0;
-#pragma unroll
-    for (int i = 0; i < m; ++i) {
-      const float send = hi ? v[i] : v[i + m];
-      const float keep = hi ? v[i + m] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-    }
-  }
+  reduce_scatter_round<LPC / 2, LPC>(v, q);
   return v[0];
 }
 
