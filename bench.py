@@ -126,12 +126,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+SCAN_KERNEL_SOURCES = ("device_common.cuh", "scan_args.h", "scan_kernel.cuh", "scan_bf16.cu", "scan_f32.cu")
+
+
 def kernel_source_sha():
-    """Hash of the CUDA sources, so that stored ncu figures are used only for the kernel they measured."""
+    """Hash of the scan kernel's sources, so that stored ncu figures are used only for the kernel they measured."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_125_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in SCAN_KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
