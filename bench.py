@@ -129,6 +129,22 @@ class ClockSampler:
 SCAN_KERNEL_SOURCES = ("device_common.cuh", "scan_args.h", "scan_kernel.cuh", "scan_bf16.cu", "scan_f32.cu")
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's figure: every rank's timed region ends at a barrier,
+    so the job's step time is the max over ranks."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Units all ranks processed per second (weak scaling: every rank runs the same workload)."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def kernel_source_sha():
     """Hash of the scan kernel's sources, so that stored ncu figures are used only for the kernel they measured."""
     import hashlib
@@ -275,14 +291,9 @@ def run_ours(args, rank, world, device):
     assert binding.mamba_device_status() == 0, "a kernel reported a timeout"
     ms_total = ev0.elapsed_time(ev1)
     scan_ms = [a.elapsed_time(b) for a, b in ev_scan]
-    ms_per_step = ms_total / K
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-
+    ms_per_step = max_over_ranks(ms_total / K, world, device)
     chsteps = B * Dm * (L + 1)
-    value = world * chsteps / (ms_per_step / 1e3)
+    value = job_rate(chsteps, world, ms_per_step)
 
     # ---- e2e through the public API with pinned host buffers
     pin = {k: v.cpu().pin_memory() for k, v in base.items()}
@@ -308,11 +319,7 @@ def run_ours(args, rank, world, device):
         host_tok_out.copy_(s["tok_out"], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1) / Ke
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / Ke, world, device)
 
     peaks = read_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -352,7 +359,7 @@ def run_ours(args, rank, world, device):
         "hbm": {"achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / peaks["hbm_gbs"], "bytes_per_launch": alg_bytes,
                 "peak_source": f"MEASURED_PEAKS.json ({peaks['source']})"},
-        "e2e": {"value": world * chsteps / (e2e_ms / 1e3), "unit": "channel-steps/s",
+        "e2e": {"value": job_rate(chsteps, world, e2e_ms), "unit": "channel-steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": K * (scan_launches + 1),
         "clocks": clocks,
