@@ -55,6 +55,7 @@ def parse():
     p.add_argument("--lanes", type=int, default=0, help="plan override: lanes per channel")
     p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
     p.add_argument("--no-decode", action="store_true", help="skip the full-size decode measurement")
+    p.add_argument("--no-variants", action="store_true", help="skip the simplified-discretisation scan timing")
     return p.parse_args()
 
 
@@ -341,6 +342,30 @@ def run_ours(args, rank, world, device):
         elif tr:
             traffic_note = "ncu summary is for another plan or an older kernel"
     decode = None if args.no_decode else measure_decode(device, stream, peaks)
+    # The same scan with the simplified discretisation (Bbar = dt B): 4 FP32 lane-ops per state.
+    simple = None
+    if not args.no_variants:
+        splan = binding.ScanPlan(chosen.lanes_per_channel, chosen.segments, 0, binding.MAMBA_SIMPLIFIED)
+        for i in range(3):
+            s = sets[i % nsets]
+            binding.mamba_selective_scan_fwd(s["u"], s["delta"], A_log, s["B"], s["C"], Dv, s["z"], bias,
+                                             s["out"], s["last"], plan=splan)
+        torch.cuda.synchronize(device)
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        nv = 50
+        v0.record(stream)
+        for i in range(nv):
+            s = sets[i % nsets]
+            binding.mamba_selective_scan_fwd(s["u"], s["delta"], A_log, s["B"], s["C"], Dv, s["z"], bias,
+                                             s["out"], s["last"], plan=splan)
+        v1.record(stream)
+        torch.cuda.synchronize(device)
+        sms_ = v0.elapsed_time(v1) / nv
+        sops = 4 * N * B * L * Dm
+        simple = {"discretization": "simplified (Bbar = dt B)", "kernel_ms": sms_,
+                  "achieved": sops / (sms_ / 1e3) / 1e12, "unit": "T FP32 lane-op/s",
+                  "frac": sops / (sms_ / 1e3) / 1e12 / peak_tops, "ops_per_launch": sops,
+                  "hbm_frac": alg_bytes / (sms_ / 1e3) / 1e9 / peaks["hbm_gbs"], "calls": nv}
     result = {
         "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -366,6 +391,8 @@ def run_ours(args, rank, world, device):
     }
     if decode is not None:
         result["decode"] = decode
+    if simple is not None:
+        result["scan_simplified"] = simple
     return result
 
 

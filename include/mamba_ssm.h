@@ -105,20 +105,38 @@ MAMBA_API mamba_status_t mamba_selective_scan_fwd(
     mamba_stream_t stream);
 
 /*
+ * Discretisation of the input matrix.
+ *   MAMBA_ZOH        : zero-order hold, Bbar = (exp(dt A) - 1) / A * B - the
+ *                      method ("State Space Models and Mamba" §2, "Mamba"
+ *                      paper notes, Design 1). The default.
+ *   MAMBA_SIMPLIFIED : Bbar = dt * B, the form of the paper notes'
+ *                      selective_ssm sketch (first order in dt A); Abar is
+ *                      still exp(dt A). About a third fewer FP32 operations.
+ */
+typedef enum {
+    MAMBA_ZOH = 0,
+    MAMBA_SIMPLIFIED = 1
+} mamba_discretization_t;
+
+/*
  * Plan knobs for mamba_selective_scan_fwd_ex. A zero field means "choose
- * automatically"; results never depend on the plan beyond fp32 rounding
- * order (the tests compare plans against each other and the oracle).
+ * automatically" (or ZOH for discretization). lanes_per_channel, segments
+ * and use_tma never change results beyond fp32 rounding order (the tests
+ * compare plans against each other and the oracle); discretization selects
+ * the input matrix.
  *   lanes_per_channel : threads sharing one channel's N states: a power of
  *                       two from ceil(N / 16) to 16;
  *   segments          : the sequence is cut into this many time segments that
  *                       run in parallel, joined by the two-pass carry (1 = off);
  *   use_tma           : 0 auto, 1 require the TMA tile loader (error if the
- *                       layout does not allow it), 2 force plain loads.
+ *                       layout does not allow it), 2 force plain loads;
+ *   discretization    : a mamba_discretization_t value.
  */
 typedef struct {
     int lanes_per_channel;
     int segments;
     int use_tma;
+    int discretization;
 } mamba_scan_plan_t;
 
 /*
@@ -170,7 +188,8 @@ MAMBA_API mamba_status_t mamba_selective_scan_fwd_noalloc(
  * current device, assuming 16-byte aligned pointers: writes the chosen knobs
  * to *chosen (use_tma = 1 if the TMA loader would be used, else 2) and the
  * number of kernel launches one call makes (1, or 2 with segments > 1) to
- * *kernel_launches. Validation and errors as for the scan itself.
+ * *kernel_launches. Validation and errors as for the scan itself; the
+ * discretization knob is copied through.
  */
 MAMBA_API mamba_status_t mamba_selective_scan_plan(
     int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
@@ -195,6 +214,16 @@ MAMBA_API mamba_status_t mamba_selective_state_update(
     float *state, const void *u, const void *delta, const float *A_log,
     const void *B, const void *C, const float *D, const void *z,
     const float *delta_bias, void *out, mamba_stream_t stream);
+
+/*
+ * As mamba_selective_state_update, with the discretisation of the input
+ * matrix (a mamba_discretization_t value; MAMBA_ERR_INVALID_ARG otherwise).
+ */
+MAMBA_API mamba_status_t mamba_selective_state_update_ex(
+    int batch, int dim, int dstate, mamba_dtype_t in_dtype,
+    float *state, const void *u, const void *delta, const float *A_log,
+    const void *B, const void *C, const float *D, const void *z,
+    const float *delta_bias, void *out, int discretization, mamba_stream_t stream);
 
 /* Static description of a status code. */
 MAMBA_API const char *mamba_status_string(mamba_status_t s);

@@ -18,6 +18,8 @@ LIB_PATH = os.path.join(_PKG, "libmamba_ssm_b300.so")
 
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
+MAMBA_ZOH = 0
+MAMBA_SIMPLIFIED = 1
 STATUS_NAMES = {0: "MAMBA_OK", 1: "MAMBA_ERR_INVALID_ARG", 2: "MAMBA_ERR_UNSUPPORTED",
                 3: "MAMBA_ERR_CUDA", 4: "MAMBA_ERR_TIMEOUT"}
 
@@ -25,16 +27,17 @@ STATUS_NAMES = {0: "MAMBA_OK", 1: "MAMBA_ERR_INVALID_ARG", 2: "MAMBA_ERR_UNSUPPO
 EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_selective_state_update", "mamba_status_string",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
-            "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc")
+            "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc",
+            "mamba_selective_state_update_ex")
 
 _lock = threading.Lock()
 _lib = None
 
 
 class ScanPlan(ctypes.Structure):
-    """mamba_scan_plan_t: 0 in a field means automatic."""
+    """mamba_scan_plan_t: 0 in a field means automatic (ZOH for discretization)."""
     _fields_ = [("lanes_per_channel", ctypes.c_int), ("segments", ctypes.c_int),
-                ("use_tma", ctypes.c_int)]
+                ("use_tma", ctypes.c_int), ("discretization", ctypes.c_int)]
 
 
 class MambaError(RuntimeError):
@@ -64,6 +67,8 @@ def library() -> ctypes.CDLL:
             lib.mamba_selective_scan_fwd_noalloc.restype = i
             lib.mamba_selective_state_update.argtypes = [i, i, i, i] + [vp] * 10 + [vp]
             lib.mamba_selective_state_update.restype = i
+            lib.mamba_selective_state_update_ex.argtypes = [i, i, i, i] + [vp] * 10 + [i, vp]
+            lib.mamba_selective_state_update_ex.restype = i
             lib.mamba_status_string.argtypes = [i]
             lib.mamba_status_string.restype = ctypes.c_char_p
             lib.mamba_last_error_detail.argtypes = []
@@ -174,9 +179,10 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
 
 
 def mamba_selective_state_update(state, u, delta, A_log, B, C, D=None, z=None, delta_bias=None,
-                                 out=None, *, stream=None):
+                                 out=None, *, discretization=MAMBA_ZOH, stream=None):
     """One decode step through the C ABI; ``state`` (batch, dim, N) float32 is
-    updated in place. u, delta, z: (batch, dim); B, C: (batch, N). Returns out."""
+    updated in place. u, delta, z: (batch, dim); B, C: (batch, N). Returns out.
+    ``discretization`` is MAMBA_ZOH (the method) or MAMBA_SIMPLIFIED."""
     torch = _torch()
     batch, dim, dstate = state.shape
     dev = state.device
@@ -194,7 +200,12 @@ def mamba_selective_state_update(state, u, delta, A_log, B, C, D=None, z=None, d
         _ptr(delta_bias, "delta_bias", (dim,), torch.float32, dev),
         _ptr(out, "out", xs, u.dtype, dev),
     ]
-    check(library().mamba_selective_state_update(batch, dim, dstate, code, *args, _stream(stream, dev)))
+    lib = library()
+    if discretization == MAMBA_ZOH:
+        check(lib.mamba_selective_state_update(batch, dim, dstate, code, *args, _stream(stream, dev)))
+    else:
+        check(lib.mamba_selective_state_update_ex(batch, dim, dstate, code, *args, int(discretization),
+                                                  _stream(stream, dev)))
     return out
 
 

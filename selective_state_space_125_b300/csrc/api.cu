@@ -17,8 +17,10 @@
 #include "scan_args.h"
 
 namespace mamba {
-cudaError_t launch_scan_f32(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
-cudaError_t launch_scan_bf16(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_f32_d0(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_f32_d1(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_bf16_d0(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_bf16_d1(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
 bool scan_variant_f32(int, int, ScanVariant*);
 bool scan_variant_bf16(int, int, ScanVariant*);
 }  // namespace mamba
@@ -123,6 +125,16 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool variant_for(int dtype, int npl, int lpc, ScanVariant* v) {
   return dtype == 0 ? scan_variant_f32(npl, lpc, v) : scan_variant_bf16(npl, lpc, v);
+}
+
+// One scan pass for (input dtype, discretisation).
+cudaError_t launch_scan_pass(int dtype, int disc, int npl, int lpc, ScanMode mode, const ScanArgs& a,
+                             const ScanMaps& maps, dim3 grid, cudaStream_t stream) {
+  if (dtype == 0)
+    return disc == 0 ? launch_scan_f32_d0(npl, lpc, mode, a, maps, grid, stream)
+                     : launch_scan_f32_d1(npl, lpc, mode, a, maps, grid, stream);
+  return disc == 0 ? launch_scan_bf16_d0(npl, lpc, mode, a, maps, grid, stream)
+                   : launch_scan_bf16_d1(npl, lpc, mode, a, maps, grid, stream);
 }
 
 // States per thread for `lpc` threads per channel: the smallest of 4, 8, 16
@@ -237,8 +249,9 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
     return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
   if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
   if (plan_knobs && (plan_knobs->lanes_per_channel < 0 || plan_knobs->segments < 0 || plan_knobs->use_tma < 0 ||
-                     plan_knobs->use_tma > 2))
+                     plan_knobs->use_tma > 2 || plan_knobs->discretization < 0 || plan_knobs->discretization > 1))
     return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
+  const int disc = plan_knobs ? plan_knobs->discretization : 0;
   if (batch == 0 || dim == 0) return MAMBA_OK;
   const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
   const size_t es = dtype == 0 ? 4 : 2;
@@ -313,8 +326,7 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
 
   auto launch = [&](ScanMode mode, unsigned nz) {
     dim3 grid((dim + cb - 1) / cb, batch, nz);
-    return dtype == 0 ? launch_scan_f32(plan.npl, plan.lpc, mode, a, maps, grid, stream)
-                      : launch_scan_bf16(plan.npl, plan.lpc, mode, a, maps, grid, stream);
+    return launch_scan_pass(dtype, disc, plan.npl, plan.lpc, mode, a, maps, grid, stream);
   };
 
   void* work = nullptr;
@@ -361,6 +373,7 @@ mamba_status_t mamba_selective_scan_plan(int batch, int dim, int dstate, int seq
   if (st != MAMBA_OK) return st;
   chosen->lanes_per_channel = plan.lpc;
   chosen->segments = plan.nseg;
+  chosen->discretization = knobs ? knobs->discretization : 0;
   chosen->use_tma = (plan.tma_x && plan.tma_bc) ? 1 : 2;
   *kernel_launches = plan.nseg > 1 ? 2 : 1;
   return MAMBA_OK;
@@ -374,11 +387,14 @@ mamba_status_t mamba_selective_scan_fwd(int batch, int dim, int dstate, int seql
                                      nullptr, out, last_state, nullptr, stream);
 }
 
-mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamba_dtype_t in_dtype, float* state,
-                                            const void* u, const void* delta, const float* A_log, const void* B,
-                                            const void* C, const float* D, const void* z, const float* delta_bias,
-                                            void* out, mamba_stream_t stream_) {
+mamba_status_t mamba_selective_state_update_ex(int batch, int dim, int dstate, mamba_dtype_t in_dtype,
+                                               float* state, const void* u, const void* delta, const float* A_log,
+                                               const void* B, const void* C, const float* D, const void* z,
+                                               const float* delta_bias, void* out, int discretization,
+                                               mamba_stream_t stream_) {
   t_detail.clear();
+  if (discretization < 0 || discretization > 1)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown discretization %d", discretization);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 0 || dim < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d)", batch, dim);
   if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
@@ -413,9 +429,18 @@ mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamb
   a.D = D;
   a.delta_bias = delta_bias;
   a.out = out;
+  a.disc = discretization;
   cudaError_t e = launch_state_update(in_dtype == MAMBA_F32 ? 0 : 1, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "state update launch");
   return MAMBA_OK;
+}
+
+mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamba_dtype_t in_dtype, float* state,
+                                            const void* u, const void* delta, const float* A_log, const void* B,
+                                            const void* C, const float* D, const void* z, const float* delta_bias,
+                                            void* out, mamba_stream_t stream) {
+  return mamba_selective_state_update_ex(batch, dim, dstate, in_dtype, state, u, delta, A_log, B, C, D, z,
+                                         delta_bias, out, 0, stream);
 }
 
 const char* mamba_status_string(mamba_status_t s) {
@@ -494,8 +519,9 @@ extern "C" mamba_status_t mamba_selective_scan_fwd_noalloc(
     return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
   if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
   if (plan_knobs && (plan_knobs->lanes_per_channel < 0 || plan_knobs->segments < 0 || plan_knobs->use_tma < 0 ||
-                     plan_knobs->use_tma > 2))
+                     plan_knobs->use_tma > 2 || plan_knobs->discretization < 0 || plan_knobs->discretization > 1))
     return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
+  const int disc = plan_knobs ? plan_knobs->discretization : 0;
   if (batch == 0 || dim == 0) return MAMBA_OK;
   const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
   const size_t es = dtype == 0 ? 4 : 2;
@@ -578,8 +604,7 @@ extern "C" mamba_status_t mamba_selective_scan_fwd_noalloc(
   a.agg_dsum = scratch + rows * dstate;   // before the full pass reads it
   auto launch = [&](ScanMode mode, unsigned nz) {
     dim3 grid((dim + cb - 1) / cb, batch, nz);
-    return dtype == 0 ? launch_scan_f32(plan.npl, plan.lpc, mode, a, maps, grid, stream)
-                      : launch_scan_bf16(plan.npl, plan.lpc, mode, a, maps, grid, stream);
+    return launch_scan_pass(dtype, disc, plan.npl, plan.lpc, mode, a, maps, grid, stream);
   };
   cudaError_t e = cudaSuccess;
   if (plan.nseg > 1) e = launch(ScanMode::kAggregate, plan.nseg - 1);

@@ -46,10 +46,6 @@ struct ScanVariant {
 
 enum class ScanMode { kFull = 0, kAggregate = 1 };
 
-// Launches one scan pass. Returns cudaSuccess or the launch error.
-// dtype: 0 = fp32 inputs (precise math), 1 = bf16 inputs (fast math).
-cudaError_t launch_scan(int dtype, int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps,
-                        dim3 grid, cudaStream_t stream);
 
 
 // Decode step.
@@ -65,6 +61,7 @@ struct DecodeArgs {
   const float* D;
   const float* delta_bias;
   void* out;
+  int disc;  // 0 = zero-order hold, 1 = simplified Bbar = dt B
 };
 cudaError_t launch_state_update(int dtype, const DecodeArgs& a, cudaStream_t stream);
 

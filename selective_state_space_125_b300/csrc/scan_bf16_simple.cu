@@ -1,0 +1,11 @@
+// bf16-input, simplified-Bbar instantiations of the scan kernels.
+#include "scan_kernel.cuh"
+
+namespace mamba {
+
+cudaError_t launch_scan_bf16_d1(int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps,
+                                dim3 grid, cudaStream_t stream) {
+  return launch_scan_typed<__nv_bfloat16, 1>(npl, lpc, mode, a, maps, grid, stream);
+}
+
+}  // namespace mamba

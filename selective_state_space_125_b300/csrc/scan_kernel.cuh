@@ -32,6 +32,10 @@
 //     the precise path on the unscaled state with expm1f, so that
 //     (Abar - 1) / A keeps full relative accuracy.
 //
+// With DISC = 1 the input matrix is the simplified Bbar = dt B of the "Mamba"
+// paper notes' selective_ssm sketch (a follow-up option, not the method's ZOH):
+// the state is kept unscaled and one step costs four FP32 lane-ops per state.
+//
 // Time segments (the split-L two-pass scheme): with nseg > 1 the aggregate
 // pass (AGG = true) runs segments 0..nseg-2 from h = 0 and writes each
 // segment's end state and sum of dt; the full pass then starts segment k from
@@ -128,6 +132,55 @@ __device__ __forceinline__ float step_precise(float2 (&h)[NPL / 2], const float2
   return y;
 }
 
+// Simplified discretisation (Bbar = dt B, the "Mamba" paper notes' selective_ssm
+// sketch), fast path on the unscaled state: h <- Abar h + (dt u) B with Abar =
+// 2^(dt * Ak), readout sum_j C_j h_j. Four FP32 lane-ops per state instead of six.
+template <int NPL, bool READ>
+__device__ __forceinline__ float step_fast_simple(float2 (&h)[NPL / 2], const float2 (&Ak)[NPL / 2], float dt,
+                                                  float u, const float* Bt, const float* Ct) {
+  const float2 dd = make_float2(dt, dt);
+  const float du = dt * u;
+  const float2 dud = make_float2(du, du);
+  float2 yy[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+  for (int j = 0; j < NPL / 2; j += 2) {
+    const float4 B4 = *reinterpret_cast<const float4*>(Bt + 2 * j);
+    float4 C4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (READ) C4 = *reinterpret_cast<const float4*>(Ct + 2 * j);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 Bp = k == 0 ? make_float2(B4.x, B4.y) : make_float2(B4.z, B4.w);
+      const float2 x = __fmul2_rn(dd, Ak[j + k]);
+      const float2 ab = make_float2(hw_ex2(x.x), hw_ex2(x.y));
+      h[j + k] = __ffma2_rn(ab, h[j + k], __fmul2_rn(Bp, dud));
+      if (READ) {
+        const float2 Cp = k == 0 ? make_float2(C4.x, C4.y) : make_float2(C4.z, C4.w);
+        yy[k] = __ffma2_rn(Cp, h[j + k], yy[k]);
+      }
+    }
+  }
+  return (yy[0].x + yy[1].x) + (yy[0].y + yy[1].y);
+}
+
+// Simplified discretisation, precise path: h <- exp(dt A) h + dt B u.
+template <int NPL, bool READ>
+__device__ __forceinline__ float step_precise_simple(float2 (&h)[NPL / 2], const float2 (&Ak)[NPL / 2], float dt,
+                                                     float u, const float* Bt, const float* Ct) {
+  float y = 0.0f;
+  const float du = dt * u;
+#pragma unroll
+  for (int j = 0; j < NPL / 2; ++j) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float A = k == 0 ? Ak[j].x : Ak[j].y;
+      float& hv = k == 0 ? h[j].x : h[j].y;
+      hv = fmaf(expf(dt * A), hv, du * Bt[2 * j + k]);
+      if (READ) y = fmaf(Ct[2 * j + k], hv, y);
+    }
+  }
+  return y;
+}
+
 // Sum over the LPC lanes of a channel of v[0..LPC), scattered so that lane q
 // returns the total of entry q: recursive halving over xor partners, one
 // round per bit of q from the highest (M = LPC / 2) down to 1. Written as a
@@ -159,12 +212,14 @@ struct ScanMinBlocks {
   static constexpr int value = NPL <= 4 ? 8 : (NPL <= 8 ? 7 : 4);
 };
 
-template <typename Tin, int NPL, int LPC, bool AGG>
+// DISC: 0 = zero-order hold (the method), 1 = simplified Bbar = dt B.
+template <typename Tin, int NPL, int LPC, bool AGG, int DISC>
 __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     scan_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
   using G = ScanGeom<Tin, NPL, LPC>;
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
+  constexpr bool SCALED = !PRECISE && DISC == 0;  // fast ZOH path keeps s = A h
   constexpr int CB = G::kCB, NP = G::kNP, CH = G::kChunk;
   constexpr int NH = NPL / 2;
 
@@ -269,7 +324,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         hin = fmaf(decay, hin, a.agg_h[(row * Dm + d) * N + n]);
       }
     }
-    const float sv = PRECISE ? hin : hin * A;  // fast path keeps s = A h
+    const float sv = SCALED ? hin * A : hin;
     if (j % 2 == 0) {
       Ak[j / 2].x = ak;
       Ik[j / 2].x = ik;
@@ -319,7 +374,11 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         const float dt = LPC == 1 ? dt_cu : __shfl_sync(0xffffffffu, dt_cu, src);
         const float u = LPC == 1 ? u_cu : __shfl_sync(0xffffffffu, u_cu, src);
         const float* Bt = bcq + (tg + j) * 2 * NP;
-        if constexpr (PRECISE)
+        if constexpr (DISC == 1 && PRECISE)
+          yp[j] = step_precise_simple<NPL, !AGG>(st, Ak, dt, u, Bt, Bt + NP);
+        else if constexpr (DISC == 1)
+          yp[j] = step_fast_simple<NPL, !AGG>(st, Ak, dt, u, Bt, Bt + NP);
+        else if constexpr (PRECISE)
           yp[j] = step_precise<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
         else
           yp[j] = step_fast<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
@@ -419,7 +478,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       const int n = q * NPL + j;
       const float sv = (j % 2 == 0) ? st[j / 2].x : st[j / 2].y;
       const float ik = (j % 2 == 0) ? Ik[j / 2].x : Ik[j / 2].y;
-      if (n < N) a.agg_h[(row * Dm + d) * N + n] = PRECISE ? sv : sv * ik;
+      if (n < N) a.agg_h[(row * Dm + d) * N + n] = SCALED ? sv * ik : sv;
     }
     if (q == 0) a.agg_dsum[row * Dm + d] = PRECISE ? float(dsum_d) : dsum;
   } else {
@@ -429,19 +488,19 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         const int n = q * NPL + j;
         const float sv = (j % 2 == 0) ? st[j / 2].x : st[j / 2].y;
         const float ik = (j % 2 == 0) ? Ik[j / 2].x : Ik[j / 2].y;
-        if (n < N) a.last_state[((size_t)b * Dm + d) * N + n] = PRECISE ? sv : sv * ik;
+        if (n < N) a.last_state[((size_t)b * Dm + d) * N + n] = SCALED ? sv * ik : sv;
       }
     }
   }
 }
 
 // Launch one (dtype, NPL, LPC, mode) instantiation.
-template <typename Tin, int NPL, int LPC>
+template <typename Tin, int DISC, int NPL, int LPC>
 cudaError_t launch_scan_variant(ScanMode mode, const ScanArgs& a, const ScanMaps& maps, dim3 grid,
                                 cudaStream_t stream) {
   using G = ScanGeom<Tin, NPL, LPC>;
-  auto kfull = scan_kernel<Tin, NPL, LPC, false>;
-  auto kagg = scan_kernel<Tin, NPL, LPC, true>;
+  auto kfull = scan_kernel<Tin, NPL, LPC, false, DISC>;
+  auto kagg = scan_kernel<Tin, NPL, LPC, true, DISC>;
   static bool configured = false;  // per instantiation; benign race (idempotent)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
@@ -481,11 +540,11 @@ void describe_variant(ScanVariant* v) {
   X(16, 8)                     \
   X(16, 16)
 
-template <typename Tin>
+template <typename Tin, int DISC>
 cudaError_t launch_scan_typed(int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps, dim3 grid,
                               cudaStream_t stream) {
 #define MAMBA_CASE(P, Q) \
-  if (npl == P && lpc == Q) return launch_scan_variant<Tin, P, Q>(mode, a, maps, grid, stream);
+  if (npl == P && lpc == Q) return launch_scan_variant<Tin, DISC, P, Q>(mode, a, maps, grid, stream);
   MAMBA_SCAN_VARIANTS(MAMBA_CASE)
 #undef MAMBA_CASE
   return cudaErrorInvalidValue;

@@ -20,6 +20,7 @@
 // 1/A; exp(dt A) - 1 comes from a four-term series when |dt A| < 1/8 (where
 // ex2 - 1 would cancel) and from ex2 - 1 otherwise, so (exp(dt A) - 1) / A
 // keeps a relative error near 1e-6. fp32 inputs use expf / expm1f / log1pf.
+// With the simplified discretisation (disc = 1) the input term is dt B u.
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -161,16 +162,23 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float x = dt * Al[k][i];
-        float ab, e;  // Abar and Abar - 1
-        if (PRECISE) {
-          e = expm1f(x);
-          ab = 1.0f + e;
+        float ab, coef;  // Abar and the factor of B u in Bbar u
+        if (a.disc == 1) {
+          // simplified discretisation: Bbar = dt B
+          ab = PRECISE ? expf(x) : hw_ex2(x);
+          coef = dt;
         } else {
-          ab = hw_ex2(x);
-          e = expm1_from_ex2(x * kLn2, ab);
+          float e;  // Abar - 1
+          if (PRECISE) {
+            e = expm1f(x);
+            ab = 1.0f + e;
+          } else {
+            ab = hw_ex2(x);
+            e = expm1_from_ex2(x * kLn2, ab);
+          }
+          // (Abar - 1) / A, with the limit dt where dt A underflows to zero
+          coef = (x != 0.0f) ? (PRECISE ? e / Al[k][i] : e * Ik[k][i]) : dt;
         }
-        // (Abar - 1) / A, with the limit dt where dt A underflows to zero
-        const float coef = (x != 0.0f) ? (PRECISE ? e / Al[k][i] : e * Ik[k][i]) : dt;
         const float Bn = VEC ? Bq[r][k].get(i) : Bs[VEC ? 0 : r][k][i];
         const float Cn = VEC ? Cq[r][k].get(i) : Cs[VEC ? 0 : r][k][i];
         hv[r][k][i] = fmaf(coef * Bn, uf[r], ab * hv[r][k][i]);

@@ -74,8 +74,15 @@ def test_scan_rejects_bad_arguments(lib, kw, status):
 
 def test_bad_plan_knobs(lib):
     from selective_state_space_125_b300.binding import ScanPlan
-    for p in (ScanPlan(-1, 0, 0), ScanPlan(0, -2, 0), ScanPlan(0, 0, 3)):
+    for p in (ScanPlan(-1, 0, 0), ScanPlan(0, -2, 0), ScanPlan(0, 0, 3), ScanPlan(0, 0, 0, 2),
+              ScanPlan(0, 0, 0, -1)):
         assert scan(lib, plan=ctypes.byref(p)) == 1
+
+
+def test_state_update_rejects_unknown_discretisation(lib):
+    assert lib.mamba_selective_state_update_ex(2, 8, 16, 1, FAKE, FAKE + 0x100000, FAKE + 0x200000,
+                                               FAKE + 0x300000, FAKE + 0x400000, FAKE + 0x500000, None, None,
+                                               None, FAKE + 0x600000, 5, None) == 1
 
 
 def test_empty_problems_are_ok_without_a_device(lib):

@@ -135,3 +135,26 @@ def test_full_size_decode_sampled(dev, name):
     rst, routs = run_decode_oracle(inp, cfg.steps, bsel=bsel, dsel=dsel)
     assert parity_err(st, rst) <= TOL[cfg.dtype], parity_err(st, rst)
     assert parity_err(outs, routs) <= TOL[cfg.dtype], parity_err(outs, routs)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [16, 128])
+def test_decode_simplified_discretisation(dev, dtype, dstate):
+    import torch
+    from selective_state_space_125_b300 import binding
+    inp = make_decode_inputs(3, 70, dstate, dtype, seed=dstate + 1, pool=3)
+    state = f32t(inp["state0"], dev)
+    A_log, D, bias = f32t(inp["A_log"], dev), f32t(inp["D"], dev), f32t(inp["delta_bias"], dev)
+    rst = inp["state0"].astype(np.float64)
+    outs, routs = [], []
+    for p in range(3):
+        t = {k: to_torch(inp[k][p], dtype, dev) for k in ("u", "delta", "z", "B", "C")}
+        outs.append(to_numpy(binding.mamba_selective_state_update(
+            state, t["u"], t["delta"], A_log, t["B"], t["C"], D, t["z"], bias,
+            discretization=binding.MAMBA_SIMPLIFIED)))
+        rst, ro = oracle.state_update(rst, inp["u"][p], inp["delta"][p], inp["A_log"], inp["B"][p], inp["C"][p],
+                                      inp["D"], inp["z"][p], inp["delta_bias"], variant=oracle.SIMPLIFIED)
+        routs.append(ro)
+    torch.cuda.synchronize()
+    assert parity_err(to_numpy(state), rst) <= TOL[dtype]
+    assert parity_err(np.stack(outs), np.stack(routs)) <= TOL[dtype]

@@ -189,3 +189,17 @@ def test_full_size_configs_sampled(dev, name):
     e1, e2 = parity_err(gout, rout), parity_err(glast, rlast)
     assert e1 <= TOL[cfg.dtype] and e2 <= TOL[cfg.dtype], f"{name}: out {e1:.2e} last {e2:.2e}"
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(last))
+
+
+# ---- simplified discretisation (Bbar = dt B), against the oracle's variant 1
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("lpc,segments", [(0, 1), (1, 3), (4, 1), (2, 2)])
+def test_simplified_discretisation(dev, dtype, lpc, segments):
+    inp = make_scan_inputs(2, 96, 16, 500, dtype, seed=12, dt_range=(1e-4, 1.0))
+    got = run_gpu(inp, dev, plan=dict(lanes_per_channel=lpc, segments=segments, use_tma=0, discretization=1))
+    ref = oracle.selective_scan(inp["u"], inp["delta"], inp["A_log"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["delta_bias"], variant=oracle.SIMPLIFIED)
+    assert_parity(got, ref, dtype, f"simplified lpc={lpc} segments={segments}")
+    # and it is a different operator from ZOH on these inputs
+    zoh = run_oracle(inp)
+    assert parity_err(got[0], zoh[0]) > 10 * TOL[dtype]
