@@ -74,6 +74,8 @@ class OracleLib:
         lib.oracle_selective_scan.restype = ctypes.c_int
         lib.oracle_state_update.argtypes = [L, L, L] + [dp] * 10 + [ctypes.c_int]
         lib.oracle_state_update.restype = ctypes.c_int
+        lib.oracle_causal_conv1d_silu.argtypes = [L, L, L, L] + [dp] * 4
+        lib.oracle_causal_conv1d_silu.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -104,6 +106,23 @@ class OracleLib:
         if rc != 0:
             raise ValueError(f"oracle_selective_scan failed with status {rc}")
         return out, last
+
+    def causal_conv1d_silu(self, x, weight, bias=None):
+        """SiLU of the causal depthwise convolution of x (batch, L, dim) with
+        weight (dim, width) and bias (dim,) or None; returns u (batch, L, dim)."""
+        x = _f64(x)
+        batch, seqlen, dim = x.shape
+        weight = _f64(weight)
+        if weight.ndim != 2 or weight.shape[0] != dim:
+            raise ValueError(f"weight must be (dim, width), got {weight.shape}")
+        width = weight.shape[1]
+        bias = _f64(bias, (dim,))
+        u = np.zeros(x.shape, np.float64)
+        rc = self.lib.oracle_causal_conv1d_silu(batch, dim, seqlen, width, _ptr(x), _ptr(weight), _ptr(bias),
+                                                _ptr(u))
+        if rc != 0:
+            raise ValueError(f"oracle_causal_conv1d_silu failed with status {rc}")
+        return u
 
     def state_update(self, state, u, delta, A_log, B, C, D=None, z=None, delta_bias=None,
                      variant: int = ZOH):
@@ -146,3 +165,8 @@ def selective_scan(*args, **kwargs):
 def state_update(*args, **kwargs):
     """Module-level shortcut for ``default().state_update``."""
     return default().state_update(*args, **kwargs)
+
+
+def causal_conv1d_silu(*args, **kwargs):
+    """Module-level shortcut for ``default().causal_conv1d_silu``."""
+    return default().causal_conv1d_silu(*args, **kwargs)

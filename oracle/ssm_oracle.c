@@ -185,3 +185,34 @@ int oracle_state_update(long batch, long dim, long dstate, double *state,
     }
     return ORACLE_OK;
 }
+
+/* Causal depthwise 1-D convolution followed by SiLU, the step in front of the
+ * scan in the Mamba block ("Mamba" paper notes, Design 3; compassingai
+ * "Mamba" §3.3; "State Space Models and Mamba", Mamba Block architecture):
+ *   u[b,t,d] = SiLU( sum_{k=0}^{width-1} w[d,k] * x[b, t-(width-1)+k, d] + bias[d] ),
+ * with x taken as zero before t = 0 (causal padding). The tap w[d, width-1]
+ * multiplies the current input. Layouts: x, u (batch, seqlen, dim); w (dim,
+ * width); bias (dim) or NULL. */
+int oracle_causal_conv1d_silu(long batch, long dim, long seqlen, long width,
+                              const double *x, const double *w,
+                              const double *bias, double *u)
+{
+    if (batch < 0 || dim < 0 || seqlen < 0 || width < 1)
+        return ORACLE_BAD_ARG;
+    if (batch == 0 || dim == 0 || seqlen == 0)
+        return ORACLE_OK;
+    if (!x || !w || !u)
+        return ORACLE_BAD_ARG;
+    for (long b = 0; b < batch; ++b)
+        for (long t = 0; t < seqlen; ++t)
+            for (long d = 0; d < dim; ++d) {
+                double acc = bias ? bias[d] : 0.0;
+                for (long k = 0; k < width; ++k) {
+                    const long ts = t - (width - 1) + k;
+                    if (ts >= 0)
+                        acc += w[d * width + k] * x[(b * seqlen + ts) * dim + d];
+                }
+                u[(b * seqlen + t) * dim + d] = oracle_silu(acc);
+            }
+    return ORACLE_OK;
+}

@@ -351,6 +351,61 @@ def pin_simplified_variant_geometric(orc, seed=10):
     return max(errs)
 
 
+def _conv_ref_numpy(x, w, bias):
+    """Causal depthwise convolution by numpy.convolve (full mode, first L
+    outputs): an independent restatement of the same definition."""
+    batch, L, dim = x.shape
+    width = w.shape[1]
+    out = np.empty_like(x)
+    for b in range(batch):
+        for d in range(dim):
+            # convolve flips its second argument; flip the taps so that
+            # w[d, width-1] meets the current input, as in the definition.
+            out[b, :, d] = np.convolve(x[b, :, d], w[d, ::-1], mode="full")[:L] + (bias[d] if bias is not None else 0.0)
+    return silu_ref(out)
+
+
+def pin_conv_identity_tap(orc, seed=11):
+    """A kernel that is 1 on the current tap and 0 elsewhere, no bias: u = SiLU(x)."""
+    rng = np.random.default_rng(seed)
+    errs = []
+    for width in (1, 2, 4):
+        x = rng.standard_normal((2, 17, 5))
+        w = np.zeros((5, width))
+        w[:, -1] = 1.0
+        errs.append(rel_err(orc.causal_conv1d_silu(x, w), silu_ref(x)))
+    return max(errs)
+
+
+def pin_conv_matches_numpy(orc, seed=12):
+    """Random taps and bias against numpy.convolve, widths 1..4."""
+    rng = np.random.default_rng(seed)
+    errs = []
+    for width in (1, 2, 3, 4):
+        x = rng.standard_normal((2, 23, 6))
+        w = rng.standard_normal((6, width))
+        bias = rng.standard_normal(6)
+        errs.append(rel_err(orc.causal_conv1d_silu(x, w, bias), _conv_ref_numpy(x, w, bias)))
+        errs.append(rel_err(orc.causal_conv1d_silu(x, w), _conv_ref_numpy(x, w, None)))
+    return max(errs)
+
+
+def pin_conv_causal_window(orc, seed=13):
+    """Perturbing x at step s changes u only at steps s .. s + width - 1."""
+    rng = np.random.default_rng(seed)
+    width, L, s = 4, 20, 7
+    x = rng.standard_normal((1, L, 3))
+    w = rng.standard_normal((3, width)) + 0.5
+    u0 = orc.causal_conv1d_silu(x, w)
+    x2 = x.copy()
+    x2[0, s] += 1.0
+    u1 = orc.causal_conv1d_silu(x2, w)
+    changed = np.any(np.abs(u1 - u0) > 0, axis=2)[0]
+    expect = np.zeros(L, bool)
+    expect[s:s + width] = True
+    return 0.0 if np.array_equal(changed, expect) else 1.0
+
+
 # name -> (function, tolerance)
 PINS = {
     "zoh_matches_ode": (pin_zoh_matches_ode, 1e-10),
@@ -364,4 +419,7 @@ PINS = {
     "continuation": (pin_continuation, 1e-12),
     "structure": (pin_structure, 1e-12),
     "simplified_variant_geometric": (pin_simplified_variant_geometric, 1e-12),
+    "conv_identity_tap": (pin_conv_identity_tap, 1e-14),
+    "conv_matches_numpy": (pin_conv_matches_numpy, 1e-12),
+    "conv_causal_window": (pin_conv_causal_window, 0.0),
 }

@@ -37,6 +37,13 @@ MUTANTS = {
     "decode_A_index": ("const double A_n = -exp(A_log[d * dstate + n]);",
                        "const double A_n = -exp(A_log[n]);"),
     "decode_state_not_decayed": ("*h = abar * (*h) + bbar * u[i];", "*h = (*h) + bbar * u[i];"),
+    "conv_taps_reversed": ("acc += w[d * width + k] * x[(b * seqlen + ts) * dim + d];",
+                           "acc += w[d * width + (width - 1 - k)] * x[(b * seqlen + ts) * dim + d];"),
+    "conv_without_silu": ("u[(b * seqlen + t) * dim + d] = oracle_silu(acc);",
+                          "u[(b * seqlen + t) * dim + d] = acc;"),
+    # circular instead of causal zero padding (every index stays inside x)
+    "conv_circular_padding": ("const long ts = t - (width - 1) + k;",
+                              "const long ts = (t - (width - 1) + k + seqlen) % seqlen;"),
 }
 
 
