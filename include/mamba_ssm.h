@@ -153,6 +153,28 @@ MAMBA_API mamba_status_t mamba_selective_scan_fwd_ex(
     float *last_state, const mamba_scan_plan_t *plan, mamba_stream_t stream);
 
 /*
+ * The scan with the step in front of it in the Mamba block fused in: the
+ * input x is passed through a causal depthwise conv1d and SiLU,
+ *     u[b,t,d] = SiLU( sum_{k<W} conv_weight[d,k] * x[b, t-(W-1)+k, d] + conv_bias[d] ),
+ * x taken as zero before t = 0 ("Mamba" paper notes, Design 3; compassingai
+ * "Mamba" §3.3; "State Space Models and Mamba", Mamba Block architecture:
+ * kernel size 4, conv then SiLU), and u feeds the scan and its D skip.
+ *   x           : (B, L, D) in_dtype, the conv input;
+ *   conv_weight : (D, W) fp32; W = conv_width in 1..4 (tap W-1 multiplies x_t);
+ *   conv_bias   : (D,) fp32 or NULL for zero.
+ * Other arguments as mamba_selective_scan_fwd_ex. Zero-order hold only
+ * (plan->discretization must be MAMBA_ZOH): MAMBA_ERR_UNSUPPORTED otherwise,
+ * and for W outside 1..4.
+ */
+MAMBA_API mamba_status_t mamba_conv1d_selective_scan_fwd(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+    const void *x, const float *conv_weight, const float *conv_bias, int conv_width,
+    const void *delta, const float *A_log, const void *B, const void *C,
+    const float *D, const void *z, const float *delta_bias,
+    const float *initial_state, void *out, float *last_state,
+    const mamba_scan_plan_t *plan, mamba_stream_t stream);
+
+/*
  * Allocation-free variant of mamba_selective_scan_fwd_ex. The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory while they run: code inside a custom allocator or a memory-pool

@@ -28,7 +28,7 @@ EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_selective_state_update", "mamba_status_string",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
             "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc",
-            "mamba_selective_state_update_ex")
+            "mamba_selective_state_update_ex", "mamba_conv1d_selective_scan_fwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -69,6 +69,9 @@ def library() -> ctypes.CDLL:
             lib.mamba_selective_state_update.restype = i
             lib.mamba_selective_state_update_ex.argtypes = [i, i, i, i] + [vp] * 10 + [i, vp]
             lib.mamba_selective_state_update_ex.restype = i
+            lib.mamba_conv1d_selective_scan_fwd.argtypes = ([i, i, i, i, i] + [vp] * 3 + [i] + [vp] * 10 +
+                                                            [ctypes.POINTER(ScanPlan), vp])
+            lib.mamba_conv1d_selective_scan_fwd.restype = i
             lib.mamba_status_string.argtypes = [i]
             lib.mamba_status_string.restype = ctypes.c_char_p
             lib.mamba_last_error_detail.argtypes = []
@@ -173,6 +176,48 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
             plan = ScanPlan(**plan)
         p = ctypes.byref(plan) if plan is not None else None
         check(lib.mamba_selective_scan_fwd_ex(batch, dim, dstate, seqlen, code, *args, h0, *outs, p, s))
+    if last_state is not None:
+        return out, last_state
+    return out
+
+
+def mamba_conv1d_selective_scan_fwd(x, conv_weight, conv_bias, delta, A_log, B, C, D=None, z=None,
+                                    delta_bias=None, out=None, last_state=None, *, return_last_state=False,
+                                    initial_state=None, plan=None, stream=None):
+    """Causal depthwise conv1d + SiLU of x fused in front of the selective scan.
+
+    x, delta, z: (batch, L, dim); B, C: (batch, L, N), all float32 or all
+    bfloat16; conv_weight (dim, W) float32 with W in 1..4; conv_bias (dim,)
+    float32 or None; other arguments as mamba_selective_scan_fwd.
+    """
+    torch = _torch()
+    batch, seqlen, dim = x.shape
+    dstate = A_log.shape[1]
+    dev = x.device
+    code = _dtype_code(x)
+    xs = (batch, seqlen, dim)
+    bcs = (batch, seqlen, dstate)
+    width = conv_weight.shape[1] if conv_weight.dim() == 2 else -1
+    if out is None:
+        out = torch.empty_like(x)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=dev)
+    args = [
+        _ptr(x, "x", xs, x.dtype, dev), _ptr(conv_weight, "conv_weight", (dim, width), torch.float32, dev),
+        _ptr(conv_bias, "conv_bias", (dim,), torch.float32, dev), width,
+        _ptr(delta, "delta", xs, x.dtype, dev), _ptr(A_log, "A_log", (dim, dstate), torch.float32, dev),
+        _ptr(B, "B", bcs, x.dtype, dev), _ptr(C, "C", bcs, x.dtype, dev),
+        _ptr(D, "D", (dim,), torch.float32, dev), _ptr(z, "z", xs, x.dtype, dev),
+        _ptr(delta_bias, "delta_bias", (dim,), torch.float32, dev),
+        _ptr(initial_state, "initial_state", (batch, dim, dstate), torch.float32, dev),
+        _ptr(out, "out", xs, x.dtype, dev),
+        _ptr(last_state, "last_state", (batch, dim, dstate), torch.float32, dev),
+    ]
+    if isinstance(plan, dict):
+        plan = ScanPlan(**plan)
+    p = ctypes.byref(plan) if plan is not None else None
+    check(library().mamba_conv1d_selective_scan_fwd(batch, dim, dstate, seqlen, code, *args, p,
+                                                    _stream(stream, dev)))
     if last_state is not None:
         return out, last_state
     return out

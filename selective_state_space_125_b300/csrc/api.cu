@@ -21,6 +21,8 @@ cudaError_t launch_scan_f32_d0(int, int, ScanMode, const ScanArgs&, const ScanMa
 cudaError_t launch_scan_f32_d1(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
 cudaError_t launch_scan_bf16_d0(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
 cudaError_t launch_scan_bf16_d1(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_f32_conv(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
+cudaError_t launch_scan_bf16_conv(int, int, ScanMode, const ScanArgs&, const ScanMaps&, dim3, cudaStream_t);
 bool scan_variant_f32(int, int, ScanVariant*);
 bool scan_variant_bf16(int, int, ScanVariant*);
 }  // namespace mamba
@@ -127,9 +129,13 @@ bool variant_for(int dtype, int npl, int lpc, ScanVariant* v) {
   return dtype == 0 ? scan_variant_f32(npl, lpc, v) : scan_variant_bf16(npl, lpc, v);
 }
 
-// One scan pass for (input dtype, discretisation).
+// One scan pass for (input dtype, discretisation); the fused-conv kernels
+// (zero-order hold only) when the arguments carry conv taps.
 cudaError_t launch_scan_pass(int dtype, int disc, int npl, int lpc, ScanMode mode, const ScanArgs& a,
                              const ScanMaps& maps, dim3 grid, cudaStream_t stream) {
+  if (a.conv_w)
+    return dtype == 0 ? launch_scan_f32_conv(npl, lpc, mode, a, maps, grid, stream)
+                      : launch_scan_bf16_conv(npl, lpc, mode, a, maps, grid, stream);
   if (dtype == 0)
     return disc == 0 ? launch_scan_f32_d0(npl, lpc, mode, a, maps, grid, stream)
                      : launch_scan_f32_d1(npl, lpc, mode, a, maps, grid, stream);
@@ -230,15 +236,14 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
   return MAMBA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
-                                           const void* u, const void* delta, const float* A_log, const void* B,
-                                           const void* C, const float* D, const void* z, const float* delta_bias,
-                                           const float* initial_state, void* out, float* last_state,
-                                           const mamba_scan_plan_t* plan_knobs, mamba_stream_t stream_) {
+// The scan entry points' common body. conv_w == nullptr: u is the scan input;
+// otherwise u holds the conv input x and the kernels compute
+// u = SiLU(causal conv1d(x; conv_w, conv_b)) on the fly.
+mamba_status_t scan_fwd_impl(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, const void* u,
+                             const void* delta, const float* A_log, const void* B, const void* C, const float* D,
+                             const void* z, const float* delta_bias, const float* initial_state, void* out,
+                             float* last_state, const mamba_scan_plan_t* plan_knobs, mamba_stream_t stream_,
+                             const float* conv_w, const float* conv_b, int conv_width) {
   t_detail.clear();
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 0 || dim < 0 || seqlen < 0)
@@ -252,6 +257,10 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
                      plan_knobs->use_tma > 2 || plan_knobs->discretization < 0 || plan_knobs->discretization > 1))
     return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
   const int disc = plan_knobs ? plan_knobs->discretization : 0;
+  if (conv_w && (conv_width < 1 || conv_width > 4))
+    return fail(MAMBA_ERR_UNSUPPORTED, "conv_width=%d must be 1..4", conv_width);
+  if (conv_w && disc != 0)
+    return fail(MAMBA_ERR_UNSUPPORTED, "the fused conv1d is built for the zero-order-hold discretisation only");
   if (batch == 0 || dim == 0) return MAMBA_OK;
   const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
   const size_t es = dtype == 0 ? 4 : 2;
@@ -271,10 +280,10 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
                 out);
   const size_t nx = (size_t)batch * seqlen * dim * es;
   const size_t nbc = (size_t)batch * seqlen * dstate * es;
-  const void* inputs[] = {u, delta, z, B, C, A_log, D, delta_bias, initial_state};
+  const void* inputs[] = {u, delta, z, B, C, A_log, D, delta_bias, initial_state, conv_w, conv_b};
   const size_t sizes[] = {nx, nx, nx, nbc, nbc, (size_t)dim * dstate * 4, (size_t)dim * 4, (size_t)dim * 4,
-                          n_state * 4};
-  for (int i = 0; i < 9; ++i) {
+                          n_state * 4, (size_t)dim * (conv_w ? conv_width : 0) * 4, (size_t)dim * 4};
+  for (int i = 0; i < 11; ++i) {
     if (overlaps(out, nx, inputs[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "out aliases input %d", i);
     if (overlaps(last_state, n_state * 4, inputs[i], sizes[i]))
       return fail(MAMBA_ERR_INVALID_ARG, "last_state aliases input %d", i);
@@ -292,7 +301,8 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
   std::memset(&maps, 0, sizeof(maps));
   const uint32_t cb = uint32_t(kScanThreads / plan.lpc);
   if (plan.tma_x) {
-    if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
+    const uint32_t urows = plan.chunk + (conv_w ? 3 : 0);  // the fused conv reads 3 steps before the chunk
+    if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, urows)) != MAMBA_OK) return st;
     if ((st = encode_3d(&maps.delta, delta, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
     if (z && (st = encode_3d(&maps.z, z, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
   }
@@ -323,6 +333,9 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
   a.tma_x = plan.tma_x;
   a.tma_bc = plan.tma_bc;
   a.status = di.status;
+  a.conv_w = conv_w;
+  a.conv_b = conv_w ? conv_b : nullptr;
+  a.conv_width = conv_w ? conv_width : 0;
 
   auto launch = [&](ScanMode mode, unsigned nz) {
     dim3 grid((dim + cb - 1) / cb, batch, nz);
@@ -350,6 +363,35 @@ mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int s
   }
   if (e != cudaSuccess) return cuda_fail(e, "scan launch");
   return MAMBA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mamba_status_t mamba_selective_scan_fwd_ex(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                           const void* u, const void* delta, const float* A_log, const void* B,
+                                           const void* C, const float* D, const void* z, const float* delta_bias,
+                                           const float* initial_state, void* out, float* last_state,
+                                           const mamba_scan_plan_t* plan_knobs, mamba_stream_t stream) {
+  return scan_fwd_impl(batch, dim, dstate, seqlen, in_dtype, u, delta, A_log, B, C, D, z, delta_bias,
+                       initial_state, out, last_state, plan_knobs, stream, nullptr, nullptr, 0);
+}
+
+mamba_status_t mamba_conv1d_selective_scan_fwd(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                               const void* x, const float* conv_weight, const float* conv_bias,
+                                               int conv_width, const void* delta, const float* A_log,
+                                               const void* B, const void* C, const float* D, const void* z,
+                                               const float* delta_bias, const float* initial_state, void* out,
+                                               float* last_state, const mamba_scan_plan_t* plan,
+                                               mamba_stream_t stream) {
+  if (!conv_weight && batch > 0 && dim > 0) {
+    t_detail.clear();
+    return fail(MAMBA_ERR_INVALID_ARG, "conv_weight is NULL");
+  }
+  return scan_fwd_impl(batch, dim, dstate, seqlen, in_dtype, x, delta, A_log, B, C, D, z, delta_bias,
+                       initial_state, out, last_state, plan, stream, conv_weight ? conv_weight : nullptr, conv_bias,
+                       conv_width);
 }
 
 mamba_status_t mamba_selective_scan_plan(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,

@@ -30,6 +30,9 @@ struct ScanArgs {
   int tma_x;                // u/delta/z tiles by TMA (else plain loads)
   int tma_bc;               // B/C tiles by TMA (else plain loads)
   int* status;              // device status word (see record_status)
+  const float* conv_w;      // (D, conv_width): fused causal conv1d taps (conv variants only)
+  const float* conv_b;      // (D) or null
+  int conv_width;           // 1..4
 };
 
 struct ScanMaps {

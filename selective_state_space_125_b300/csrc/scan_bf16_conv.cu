@@ -1,0 +1,11 @@
+// bf16-input zero-order-hold scan kernels with the causal conv1d + SiLU fused in front.
+#include "scan_kernel.cuh"
+
+namespace mamba {
+
+cudaError_t launch_scan_bf16_conv(int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps,
+                                 dim3 grid, cudaStream_t stream) {
+  return launch_scan_typed<__nv_bfloat16, 0, true>(npl, lpc, mode, a, maps, grid, stream);
+}
+
+}  // namespace mamba

@@ -32,6 +32,11 @@
 //     the precise path on the unscaled state with expm1f, so that
 //     (Abar - 1) / A keeps full relative accuracy.
 //
+// With CONV the kernel also runs the step in front of the scan in the Mamba
+// block: u = SiLU(causal depthwise conv1d(x) + bias), width <= 4 ("Mamba"
+// paper notes, Design 3; compassingai "Mamba" §3.3), from a u tile that TMA
+// starts kConvHalo rows before the chunk (rows before t = 0 read as zero).
+//
 // With DISC = 1 the input matrix is the simplified Bbar = dt B of the "Mamba"
 // paper notes' selective_ssm sketch (a follow-up option, not the method's ZOH):
 // the state is kept unscaled and one step costs four FP32 lane-ops per state.
@@ -54,15 +59,20 @@ namespace mamba {
 
 constexpr size_t scan_a128(size_t x) { return (x + 127) & ~size_t(127); }
 
-template <typename Tin, int NPL, int LPC>
+// Steps of input before a chunk that the fused causal conv1d reads (width <= 4).
+constexpr int kConvHalo = 3;
+
+template <typename Tin, int NPL, int LPC, bool CONV = false>
 struct ScanGeom {
   static constexpr int kCB = kScanThreads / LPC;  // channels per CTA
   static constexpr int kNP = NPL * LPC;           // padded state count
   static constexpr int kES = int(sizeof(Tin));
   static constexpr int kChunk = 16;               // steps per pipeline stage (a multiple of LPC)
+  static constexpr int kURows = kChunk + (CONV ? kConvHalo : 0);  // rows of the u (or conv input) tile
+  static constexpr size_t kUTile = scan_a128(size_t(kURows) * kCB * kES);
   static constexpr size_t kXTile = scan_a128(size_t(kChunk) * kCB * kES);
   static constexpr size_t kBCTile = scan_a128(size_t(kChunk) * kNP * kES);
-  static constexpr size_t kStage = 3 * kXTile + 2 * kBCTile;
+  static constexpr size_t kStage = kUTile + 2 * kXTile + 2 * kBCTile;
   static constexpr size_t kBC32 = scan_a128(size_t(kChunk) * 2 * kNP * 4);  // [t][B | C][NP] fp32, x2 buffers
   static constexpr size_t kChan = scan_a128(size_t(kCB) * 2 * 4);           // bias, D per channel
   static constexpr size_t kBar = 128;
@@ -213,10 +223,12 @@ struct ScanMinBlocks {
 };
 
 // DISC: 0 = zero-order hold (the method), 1 = simplified Bbar = dt B.
-template <typename Tin, int NPL, int LPC, bool AGG, int DISC>
+// CONV: the u argument holds the conv input x; u = SiLU(causal conv1d(x)) is
+// computed on the fly (conv_w, conv_b, conv_width of ScanArgs).
+template <typename Tin, int NPL, int LPC, bool AGG, int DISC, bool CONV>
 __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     scan_kernel(const ScanArgs a, const __grid_constant__ ScanMaps maps) {
-  using G = ScanGeom<Tin, NPL, LPC>;
+  using G = ScanGeom<Tin, NPL, LPC, CONV>;
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
   constexpr bool SCALED = !PRECISE && DISC == 0;  // fast ZOH path keeps s = A h
@@ -230,11 +242,16 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   float* chan_D = chan_bias + CB;
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + G::kOffBar);
 
+  // Stage s: u tile (kURows rows; with CONV its first kConvHalo rows are the
+  // inputs before the chunk), delta and z tiles, B and C tiles.
   auto xu = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage); };
-  auto xd = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kXTile); };
-  auto xz = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 2 * G::kXTile); };
-  auto braw = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 3 * G::kXTile); };
-  auto craw = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + 3 * G::kXTile + G::kBCTile); };
+  auto xd = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kUTile); };
+  auto xz = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kUTile + G::kXTile); };
+  auto braw = [&](int s) { return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kUTile + 2 * G::kXTile); };
+  auto craw = [&](int s) {
+    return reinterpret_cast<Tin*>(smem + s * G::kStage + G::kUTile + 2 * G::kXTile + G::kBCTile);
+  };
+  constexpr int UH = CONV ? kConvHalo : 0;  // halo rows at the top of the u tile
   auto bc32 = [&](int k) { return reinterpret_cast<float*>(smem + G::kOffBC32 + (k & 1) * G::kBC32); };
 
   const int tid = threadIdx.x;
@@ -268,11 +285,11 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     const int s = k % kScanStages;
     const int t0 = t_begin + k * CH;
     uint32_t bytes = 0;
-    if (a.tma_x) bytes += (has_z ? 3u : 2u) * uint32_t(CH * CB * sizeof(Tin));
+    if (a.tma_x) bytes += uint32_t(((has_z ? 2 : 1) * CH + G::kURows) * CB * sizeof(Tin));
     if (a.tma_bc) bytes += 2u * uint32_t(CH * N * sizeof(Tin));
     mbar_arrive_expect_tx(&mbar[s], bytes);
     if (a.tma_x) {
-      tma_load_3d(xu(s), &maps.u, d0, t0, b, &mbar[s]);
+      tma_load_3d(xu(s), &maps.u, d0, t0 - UH, b, &mbar[s]);  // rows before 0 read as zero
       tma_load_3d(xd(s), &maps.delta, d0, t0, b, &mbar[s]);
       if (has_z) tma_load_3d(xz(s), &maps.z, d0, t0, b, &mbar[s]);
     }
@@ -337,6 +354,21 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   }
   const float bias = chan_bias[c];
   const float Dd = chan_D[c];
+  // Conv taps aligned to the u tile: tap j multiplies row tm + j (input step
+  // t - kConvHalo + j), so a width-W kernel fills taps kConvHalo + 1 - W .. kConvHalo.
+  float cw[kConvHalo + 1] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float cb = 0.0f;
+  if constexpr (CONV) {
+    if (dvalid) {
+      const int W = a.conv_width;
+#pragma unroll
+      for (int j = 0; j <= kConvHalo; ++j) {
+        const int k = j - (kConvHalo + 1 - W);
+        cw[j] = (k >= 0) ? a.conv_w[(size_t)d * W + k] : 0.0f;
+      }
+      cb = a.conv_b ? a.conv_b[d] : 0.0f;
+    }
+  }
 
   float dsum = 0.0f;    // AGG: sum of dt over the segment (fast path)
   double dsum_d = 0.0;  // AGG: the same in fp64 (precise path)
@@ -351,7 +383,15 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     (void)gout;
     // dt and u of step q of the first group, computed by this lane
     auto lane_dtu = [&](int tm, float& dtv, float& uv) {
-      const float um = E::load(su + tm * CB);
+      float um;
+      if constexpr (CONV) {
+        float acc = cb;
+#pragma unroll
+        for (int j = 0; j <= kConvHalo; ++j) acc = fmaf(cw[j], E::load(su + (tm + j) * CB), acc);
+        um = PRECISE ? silu_precise(acc) : silu_fast(acc);
+      } else {
+        um = E::load(su + tm * CB);
+      }
       const float xm = E::load(sd + tm * CB) + bias;
       const float dt = PRECISE ? softplus_precise(xm) : softplus_fast(xm);
       const bool live = tm < tv;
@@ -423,12 +463,17 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     }
     // Plain loads into the tiles where TMA cannot be used (zero outside the tensor).
     if (!a.tma_x) {
+      for (int i = tid; i < G::kURows * CB; i += kScanThreads) {
+        const int t = i / CB, cc = i % CB;
+        const int gt = t0 - UH + t, gd = d0 + cc;
+        const bool in = gt >= 0 && gt < L && gd < Dm;
+        xu(s)[i] = in ? gu[((size_t)b * L + gt) * Dm + gd] : Tin(0.0f);
+      }
       for (int i = tid; i < CH * CB; i += kScanThreads) {
         const int t = i / CB, cc = i % CB;
         const int gt = t0 + t, gd = d0 + cc;
         const bool in = gt < L && gd < Dm;
         const size_t off = ((size_t)b * L + gt) * Dm + gd;
-        xu(s)[i] = in ? gu[off] : Tin(0.0f);
         xd(s)[i] = in ? gdl[off] : Tin(0.0f);
         if (has_z) xz(s)[i] = in ? gz[off] : Tin(0.0f);
       }
@@ -495,12 +540,12 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
 }
 
 // Launch one (dtype, NPL, LPC, mode) instantiation.
-template <typename Tin, int DISC, int NPL, int LPC>
+template <typename Tin, int DISC, bool CONV, int NPL, int LPC>
 cudaError_t launch_scan_variant(ScanMode mode, const ScanArgs& a, const ScanMaps& maps, dim3 grid,
                                 cudaStream_t stream) {
-  using G = ScanGeom<Tin, NPL, LPC>;
-  auto kfull = scan_kernel<Tin, NPL, LPC, false, DISC>;
-  auto kagg = scan_kernel<Tin, NPL, LPC, true, DISC>;
+  using G = ScanGeom<Tin, NPL, LPC, CONV>;
+  auto kfull = scan_kernel<Tin, NPL, LPC, false, DISC, CONV>;
+  auto kagg = scan_kernel<Tin, NPL, LPC, true, DISC, CONV>;
   static bool configured = false;  // per instantiation; benign race (idempotent)
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kfull, cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
@@ -540,11 +585,11 @@ void describe_variant(ScanVariant* v) {
   X(16, 8)                     \
   X(16, 16)
 
-template <typename Tin, int DISC>
+template <typename Tin, int DISC, bool CONV = false>
 cudaError_t launch_scan_typed(int npl, int lpc, ScanMode mode, const ScanArgs& a, const ScanMaps& maps, dim3 grid,
                               cudaStream_t stream) {
 #define MAMBA_CASE(P, Q) \
-  if (npl == P && lpc == Q) return launch_scan_variant<Tin, DISC, P, Q>(mode, a, maps, grid, stream);
+  if (npl == P && lpc == Q) return launch_scan_variant<Tin, DISC, CONV, P, Q>(mode, a, maps, grid, stream);
   MAMBA_SCAN_VARIANTS(MAMBA_CASE)
 #undef MAMBA_CASE
   return cudaErrorInvalidValue;

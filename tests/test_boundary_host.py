@@ -115,3 +115,15 @@ def test_binding_rejects_host_tensors():
         binding.mamba_selective_scan_fwd(x, x, torch.zeros(8, 16), torch.zeros(1, 4, 16), torch.zeros(1, 4, 16))
     with pytest.raises(TypeError):
         binding.mamba_selective_scan_fwd(x.double(), x, torch.zeros(8, 16), x, x)
+
+
+def test_conv_scan_rejects_bad_arguments(lib):
+    from selective_state_space_125_b300.binding import ScanPlan
+    args = lambda width, w=FAKE + 0x700000, plan=None: (2, 8, 16, 4, 1, FAKE, w, None, width, FAKE + 0x100000,
+                                                        FAKE + 0x200000, FAKE + 0x300000, FAKE + 0x400000, None,
+                                                        None, None, None, FAKE + 0x500000, None, plan, None)
+    assert lib.mamba_conv1d_selective_scan_fwd(*args(5)) == 2          # width > 4
+    assert lib.mamba_conv1d_selective_scan_fwd(*args(0)) == 2          # width < 1
+    assert lib.mamba_conv1d_selective_scan_fwd(*args(4, w=None)) == 1  # no taps
+    p = ScanPlan(0, 0, 0, 1)
+    assert lib.mamba_conv1d_selective_scan_fwd(*args(4, plan=ctypes.byref(p))) == 2  # simplified + conv

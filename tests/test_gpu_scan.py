@@ -203,3 +203,73 @@ def test_simplified_discretisation(dev, dtype, lpc, segments):
     # and it is a different operator from ZOH on these inputs
     zoh = run_oracle(inp)
     assert parity_err(got[0], zoh[0]) > 10 * TOL[dtype]
+
+
+# ---- causal conv1d + SiLU fused in front of the scan, against oracle conv then oracle scan
+def conv_inputs(batch, dim, seqlen, width, dtype, seed, with_bias=True):
+    inp = make_scan_inputs(batch, dim, 16, seqlen, dtype, seed=seed)
+    rng = np.random.default_rng([seed, 99])
+    inp["conv_w"] = (rng.standard_normal((dim, width)) * 0.5).astype(np.float32)
+    inp["conv_b"] = rng.standard_normal(dim).astype(np.float32) if with_bias else None
+    return inp
+
+
+def run_gpu_conv(inp, dev, plan=None):
+    import torch
+    from selective_state_space_125_b300 import binding
+    t = upload_scan(inp, dev)
+    f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    out, last = binding.mamba_conv1d_selective_scan_fwd(
+        t["u"], f32(inp["conv_w"]), f32(inp["conv_b"]), t["delta"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+        t["delta_bias"], return_last_state=True, plan=plan)
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    return to_numpy(out), to_numpy(last)
+
+
+def run_oracle_conv(inp):
+    u = oracle.causal_conv1d_silu(inp["u"], inp["conv_w"], inp["conv_b"])
+    return oracle.selective_scan(u, inp["delta"], inp["A_log"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                 inp["delta_bias"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("width", [1, 2, 3, 4])
+def test_conv_scan_widths(dev, dtype, width):
+    inp = conv_inputs(2, 96, 300, width, dtype, seed=20 + width)
+    assert_parity(run_gpu_conv(inp, dev), run_oracle_conv(inp), dtype, f"conv width {width}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("plan", [dict(lanes_per_channel=1, segments=3, use_tma=0),
+                                  dict(lanes_per_channel=4, segments=2, use_tma=0),
+                                  dict(lanes_per_channel=2, segments=1, use_tma=2),
+                                  dict(lanes_per_channel=0, segments=5, use_tma=1)])
+def test_conv_scan_plans_and_segment_halos(dev, dtype, plan):
+    """Time segments start mid-sequence, where the conv reads the 3 steps before the segment."""
+    inp = conv_inputs(2, 128, 700, 4, dtype, seed=31)
+    assert_parity(run_gpu_conv(inp, dev, plan=plan), run_oracle_conv(inp), dtype, f"conv plan {plan}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_conv_scan_ragged_plain_loads_no_bias(dev, dtype):
+    inp = conv_inputs(3, 60, 37, 4, dtype, seed=33, with_bias=False)   # dim*2 = 120 bytes: plain loads for bf16
+    assert_parity(run_gpu_conv(inp, dev), run_oracle_conv(inp), dtype, "conv ragged")
+
+
+def test_conv_scan_m130_sampled(dev):
+    """The Mamba-130M-shaped layer through the fused path, sampled channels against the oracle."""
+    cfg = SCAN_CONFIGS["m130"]
+    inp = make_config_inputs(cfg, seed=1)
+    rng = np.random.default_rng(5)
+    inp["conv_w"] = (rng.standard_normal((cfg.dim, 4)) * 0.5).astype(np.float32)
+    inp["conv_b"] = rng.standard_normal(cfg.dim).astype(np.float32)
+    out, last = run_gpu_conv(inp, dev)
+    bs = np.array([0, cfg.batch - 1])
+    ds = np.unique(np.concatenate([[0, cfg.dim - 1], rng.integers(0, cfg.dim, 14)]))
+    sub = {k: inp[k][bs][:, :, ds] for k in ("u", "delta", "z")}
+    u = oracle.causal_conv1d_silu(sub["u"], inp["conv_w"][ds], inp["conv_b"][ds])
+    rout, rlast = oracle.selective_scan(u, sub["delta"], inp["A_log"][ds], inp["B"][bs], inp["C"][bs],
+                                        inp["D"][ds], sub["z"], inp["delta_bias"][ds])
+    assert parity_err(out[bs][:, :, ds], rout) <= TOL["bf16"]
+    assert parity_err(last[bs][:, ds], rlast) <= TOL["bf16"]
