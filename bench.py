@@ -56,6 +56,10 @@ def parse():
     p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
     p.add_argument("--no-decode", action="store_true", help="skip the full-size decode measurement")
     p.add_argument("--no-variants", action="store_true", help="skip the simplified-discretisation scan timing")
+    p.add_argument("--decode-only", action="store_true",
+                   help="time only the decode step on the full decode workloads and print their JSON")
+    p.add_argument("--decode-workload", default="both", choices=["both", "decode", "decode128"])
+    p.add_argument("--decode-calls", type=int, default=200)
     return p.parse_args()
 
 
@@ -130,6 +134,10 @@ class ClockSampler:
 SCAN_KERNEL_SOURCES = ("device_common.cuh", "scan_args.h", "scan_kernel.cuh", "scan_bf16.cu", "scan_f32.cu")
 
 
+def decode_names(args):
+    return ("decode", "decode128") if args.decode_workload == "both" else (args.decode_workload,)
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The slowest rank's figure: every rank's timed region ends at a barrier,
     so the job's step time is the max over ranks."""
@@ -157,7 +165,7 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
-def measure_decode(device, stream, peaks, calls=200):
+def measure_decode(device, stream, peaks, calls=200, which=("decode", "decode128")):
     """Decode step on the full decode workloads (B128 D5120, N = 16 and 128): us per call and GB/s.
 
     Each call reads and writes the resident fp32 state and reads one token's
@@ -168,7 +176,7 @@ def measure_decode(device, stream, peaks, calls=200):
     from selective_state_space_125_b300 import binding
     from selective_state_space_125_b300.workloads import DECODE_CONFIGS, make_decode_config_inputs
     out = {}
-    for name in ("decode", "decode128"):
+    for name in which:
         cfg = DECODE_CONFIGS[name]
         inp = make_decode_config_inputs(cfg, seed=0)
         B, Dm, N = cfg.batch, cfg.dim, cfg.dstate
@@ -363,7 +371,7 @@ def run_ours(args, rank, world, device):
             traffic, traffic_note = tr.get("dram_bytes_per_call"), tr.get("source")
         elif tr:
             traffic_note = "ncu summary is for another plan or an older kernel"
-    decode = None if args.no_decode else measure_decode(device, stream, peaks)
+    decode = None if args.no_decode else measure_decode(device, stream, peaks, args.decode_calls, decode_names(args))
     # The same scan with the simplified discretisation (Bbar = dt B): 4 FP32 lane-ops per state.
     simple = None
     if not args.no_variants:
@@ -535,6 +543,12 @@ def main():
         build.build()
     if world > 1:
         torch.distributed.barrier()
+    if args.decode_only:
+        out = measure_decode(device, torch.cuda.current_stream(device), read_peaks(), args.decode_calls,
+                             decode_names(args))
+        if rank == 0:
+            print(json.dumps({"decode": out}), flush=True)
+        return
     result = run_ours(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
