@@ -472,6 +472,11 @@ mamba_status_t mamba_selective_state_update_ex(int batch, int dim, int dstate, m
   a.delta_bias = delta_bias;
   a.out = out;
   a.disc = discretization;
+  DeviceInfo di;
+  const mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  a.status = di.status;
+  a.sms = di.sms;
   cudaError_t e = launch_state_update(in_dtype == MAMBA_F32 ? 0 : 1, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "state update launch");
   return MAMBA_OK;

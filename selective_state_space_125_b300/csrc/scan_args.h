@@ -64,7 +64,9 @@ struct DecodeArgs {
   const float* D;
   const float* delta_bias;
   void* out;
-  int disc;  // 0 = zero-order hold, 1 = simplified Bbar = dt B
+  int disc;     // 0 = zero-order hold, 1 = simplified Bbar = dt B
+  int* status;  // device status word (see record_status)
+  int sms;      // multiprocessors of the device
 };
 cudaError_t launch_state_update(int dtype, const DecodeArgs& a, cudaStream_t stream);
 

@@ -158,3 +158,35 @@ def test_decode_simplified_discretisation(dev, dtype, dstate):
     torch.cuda.synchronize()
     assert parity_err(to_numpy(state), rst) <= TOL[dtype]
     assert parity_err(np.stack(outs), np.stack(routs)) <= TOL[dtype]
+
+
+# ---- the bulk-staged decode path (N a power of two from 8 to 256, dim % 8 == 0)
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("dim", [136, 40])
+def test_decode_bulk_path(dev, dtype, dstate, dim):
+    """dim 136: a ragged last channel block; batch 5: row groups of unequal length; 9 steps."""
+    inp = make_decode_inputs(5, dim, dstate, dtype, seed=dstate + dim, pool=4)
+    st, outs = run_decode(inp, dev, 9)
+    rst, routs = run_decode_oracle(inp, 9)
+    assert parity_err(st, rst) <= TOL[dtype]
+    assert parity_err(outs, routs) <= TOL[dtype]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_bulk_path_simplified_and_no_gate(dev, dtype):
+    import torch
+    from selective_state_space_125_b300 import binding
+    inp = make_decode_inputs(3, 64, 16, dtype, seed=77, pool=2)
+    state = f32t(inp["state0"], dev)
+    A_log = f32t(inp["A_log"], dev)
+    rst = inp["state0"].astype(np.float64)
+    for p in range(2):
+        t = {k: to_torch(inp[k][p], dtype, dev) for k in ("u", "delta", "B", "C")}
+        y = binding.mamba_selective_state_update(state, t["u"], t["delta"], A_log, t["B"], t["C"],
+                                                 discretization=binding.MAMBA_SIMPLIFIED)
+        rst, ry = oracle.state_update(rst, inp["u"][p], inp["delta"][p], inp["A_log"], inp["B"][p], inp["C"][p],
+                                      variant=oracle.SIMPLIFIED)
+    torch.cuda.synchronize()
+    assert parity_err(to_numpy(state), rst) <= TOL[dtype]
+    assert parity_err(to_numpy(y), ry) <= TOL[dtype]
