@@ -14,6 +14,7 @@
 #include <string>
 
 #include "mamba_ssm.h"
+#include "decode_args.h"
 #include "scan_args.h"
 
 namespace mamba {

@@ -1,5 +1,5 @@
-// Host/device argument blocks and launcher declarations shared by api.cu and
-// the kernel translation units. Not part of the public ABI.
+// Host/device argument blocks of the scan kernels, shared by api.cu and the
+// scan translation units. Not part of the public ABI.
 #pragma once
 
 #include <cuda.h>
@@ -48,26 +48,5 @@ struct ScanVariant {
 };
 
 enum class ScanMode { kFull = 0, kAggregate = 1 };
-
-
-
-// Decode step.
-struct DecodeArgs {
-  int batch, dim, dstate;
-  float* state;
-  const void* u;
-  const void* delta;
-  const void* z;
-  const void* B;
-  const void* C;
-  const float* A_log;
-  const float* D;
-  const float* delta_bias;
-  void* out;
-  int disc;     // 0 = zero-order hold, 1 = simplified Bbar = dt B
-  int* status;  // device status word (see record_status)
-  int sms;      // multiprocessors of the device
-};
-cudaError_t launch_state_update(int dtype, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace mamba

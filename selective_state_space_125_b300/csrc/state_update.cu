@@ -25,7 +25,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
-#include "scan_args.h"
+#include "decode_args.h"
 
 namespace mamba {
 
