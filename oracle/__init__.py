@@ -1,4 +1,4 @@
-"""fp64 CPU oracle for the selective state-space scan and the decode step.
+"""fp64 CPU oracle for the selective state-space scan, its gradients and the decode step.
 
 TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package. It shares no code with
@@ -76,6 +76,8 @@ class OracleLib:
         lib.oracle_state_update.restype = ctypes.c_int
         lib.oracle_causal_conv1d_silu.argtypes = [L, L, L, L] + [dp] * 4
         lib.oracle_causal_conv1d_silu.restype = ctypes.c_int
+        lib.oracle_selective_scan_bwd.argtypes = [L, L, L, L] + [dp] * 20 + [ctypes.c_int]
+        lib.oracle_selective_scan_bwd.restype = ctypes.c_int
         self.lib = lib
         self.path = path
 
@@ -106,6 +108,41 @@ class OracleLib:
         if rc != 0:
             raise ValueError(f"oracle_selective_scan failed with status {rc}")
         return out, last
+
+    def selective_scan_bwd(self, u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
+                           h0=None, dlast=None, variant: int = ZOH):
+        """fp64 gradients of sum(dout * out) + sum(dlast * last_state) with respect to
+        every input of ``selective_scan``. Returns a dict with keys du, ddelta, dA_log,
+        dB, dC, and dD, dz, ddelta_bias, dh0 for the optional inputs that were given
+        (None otherwise). Shapes as in ``selective_scan``; dout like u, dlast like h0.
+        """
+        u = _f64(u)
+        batch, seqlen, dim = u.shape
+        A_log = _f64(A_log)
+        dstate = A_log.shape[1]
+        delta = _f64(delta, u.shape)
+        B = _f64(B, (batch, seqlen, dstate))
+        C = _f64(C, (batch, seqlen, dstate))
+        dout = _f64(dout, u.shape)
+        D = _f64(D, (dim,))
+        z = _f64(z, u.shape)
+        delta_bias = _f64(delta_bias, (dim,))
+        h0 = _f64(h0, (batch, dim, dstate))
+        dlast = _f64(dlast, (batch, dim, dstate))
+        g = {"du": np.zeros(u.shape), "ddelta": np.zeros(u.shape), "dA_log": np.zeros((dim, dstate)),
+             "dB": np.zeros(B.shape), "dC": np.zeros(C.shape),
+             "dD": np.zeros(dim) if D is not None else None,
+             "dz": np.zeros(u.shape) if z is not None else None,
+             "ddelta_bias": np.zeros(dim) if delta_bias is not None else None,
+             "dh0": np.zeros((batch, dim, dstate)) if h0 is not None else None}
+        rc = self.lib.oracle_selective_scan_bwd(
+            batch, dim, dstate, seqlen, _ptr(u), _ptr(delta), _ptr(A_log), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+            _ptr(delta_bias), _ptr(h0), _ptr(dout), _ptr(dlast), _ptr(g["du"]), _ptr(g["ddelta"]),
+            _ptr(g["dA_log"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]), _ptr(g["dz"]),
+            _ptr(g["ddelta_bias"]), _ptr(g["dh0"]), int(variant))
+        if rc != 0:
+            raise ValueError(f"oracle_selective_scan_bwd failed with status {rc}")
+        return g
 
     def causal_conv1d_silu(self, x, weight, bias=None):
         """SiLU of the causal depthwise convolution of x (batch, L, dim) with
@@ -165,6 +202,11 @@ def selective_scan(*args, **kwargs):
 def state_update(*args, **kwargs):
     """Module-level shortcut for ``default().state_update``."""
     return default().state_update(*args, **kwargs)
+
+
+def selective_scan_bwd(*args, **kwargs):
+    """Module-level shortcut for ``default().selective_scan_bwd``."""
+    return default().selective_scan_bwd(*args, **kwargs)
 
 
 def causal_conv1d_silu(*args, **kwargs):

@@ -1,5 +1,6 @@
 /*
- * Sequential fp64 oracle for the Mamba selective state-space scan and its
+ * Sequential fp64 oracle for the Mamba selective state-space scan, its
+ * gradients (reverse-mode differentiation of the same recurrence) and its
  * single-token decode step.
  *
  * TEST INFRASTRUCTURE ONLY. This file is the slow, obviously correct CPU
@@ -214,5 +215,185 @@ int oracle_causal_conv1d_silu(long batch, long dim, long seqlen, long width,
                 }
                 u[(b * seqlen + t) * dim + d] = oracle_silu(acc);
             }
+    return ORACLE_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Backward of the scan: the gradient of a scalar loss
+ *     loss = sum_{b,t,d} dout[b,t,d] * out[b,t,d] + sum_{b,d,n} dlast[b,d,n] * last_state[b,d,n]
+ * with respect to every input of oracle_selective_scan. The pages give the
+ * forward recurrence only; this is the chain rule applied to it in reverse
+ * time (reverse-mode differentiation of the loop above, step by step), with
+ * the forward states of each channel kept in full (no recomputation).
+ *
+ * Derivatives used (x = delta + bias, dt = softplus(x), A = -exp(A_log),
+ * abar = exp(dt A), and for zero-order hold bbar = expm1(dt A) / A * B):
+ *   d softplus(x) / dx   = sigmoid(x)
+ *   d abar / d dt        = A abar,           d abar / dA = dt abar
+ *   d bbar / d dt        = abar B            (simplified: B)
+ *   d bbar / dA          = B dt^2 phi'(dt A) (simplified: 0), where
+ *                          phi(s) = expm1(s) / s and phi'(s) = (s e^s - expm1(s)) / s^2
+ *   d A / d A_log        = A
+ *   d SiLU(z) / dz       = sigmoid(z) (1 + z (1 - sigmoid(z)))
+ *
+ * Outputs (all written, none accumulated into): du, ddelta, dz like u;
+ * dB, dC like B; dA_log like A_log; dD, ddelta_bias (dim); dh0 like h0.
+ * dz, dD, ddelta_bias and dh0 may be NULL (not computed); dlast may be NULL
+ * (zero). Sequential: the cross-channel sums (dB, dC) and the cross-batch
+ * sums (dA_log, dD, ddelta_bias) are plain running sums.
+ * ------------------------------------------------------------------------ */
+
+static double oracle_sigmoid(double x)
+{
+    return 1.0 / (1.0 + exp(-x));
+}
+
+/* phi'(s) for phi(s) = expm1(s) / s. Below |s| = 1e-3 the closed form cancels,
+ * so the Taylor series sum_k (k + 1) s^k / (k + 2)! is used (terms to s^4;
+ * the next term is below 1e-17). */
+static double oracle_dphi(double s)
+{
+    if (fabs(s) < 1e-3)
+        return 0.5 + s * (1.0 / 3.0 + s * (1.0 / 8.0 + s * (1.0 / 30.0 + s * (1.0 / 144.0))));
+    return (s * exp(s) - expm1(s)) / (s * s);
+}
+
+int oracle_selective_scan_bwd(long batch, long dim, long dstate, long seqlen,
+                              const double *u, const double *delta,
+                              const double *A_log, const double *B, const double *C,
+                              const double *D, const double *z,
+                              const double *delta_bias, const double *h0,
+                              const double *dout, const double *dlast,
+                              double *du, double *ddelta, double *dA_log,
+                              double *dB, double *dC, double *dD, double *dz,
+                              double *ddelta_bias, double *dh0, int variant)
+{
+    if (batch < 0 || dim < 0 || dstate <= 0 || seqlen < 0 || dstate > ORACLE_MAX_DSTATE)
+        return ORACLE_BAD_ARG;
+    if (!A_log || !dA_log)
+        return ORACLE_BAD_ARG;
+    if (seqlen > 0 && (!u || !delta || !B || !C || !dout || !du || !ddelta || !dB || !dC))
+        return ORACLE_BAD_ARG;
+    for (long k = 0; k < dim * dstate; ++k)
+        dA_log[k] = 0.0;
+    for (long k = 0; k < batch * seqlen * dstate; ++k)
+        dB[k] = dC[k] = 0.0;
+    for (long d = 0; d < dim; ++d) {
+        if (dD)
+            dD[d] = 0.0;
+        if (ddelta_bias)
+            ddelta_bias[d] = 0.0;
+    }
+    if (batch == 0 || dim == 0)
+        return ORACLE_OK;
+
+    /* forward record of one channel: h after each step (hs[t+1]), h0 in hs[0] */
+    double *hs = malloc(sizeof(double) * (size_t)(seqlen + 1) * (size_t)dstate);
+    double *dts = malloc(sizeof(double) * (size_t)(seqlen + 1));
+    double *ys = malloc(sizeof(double) * (size_t)(seqlen + 1));
+    if (!hs || !dts || !ys) {
+        free(hs);
+        free(dts);
+        free(ys);
+        return ORACLE_BAD_ARG;
+    }
+    double A[ORACLE_MAX_DSTATE], hbar[ORACLE_MAX_DSTATE], Abar_acc[ORACLE_MAX_DSTATE];
+
+    for (long b = 0; b < batch; ++b) {
+        for (long d = 0; d < dim; ++d) {
+            const double bias_d = (delta_bias != NULL) ? delta_bias[d] : 0.0;
+            const double *A_log_d = A_log + d * dstate;
+            for (long n = 0; n < dstate; ++n) {
+                A[n] = -exp(A_log_d[n]);
+                hs[n] = h0 ? h0[(b * dim + d) * dstate + n] : 0.0;
+            }
+            /* forward, as in oracle_scan_channel, recording h_t, dt_t and the
+             * pre-gate y_t */
+            for (long t = 0; t < seqlen; ++t) {
+                const long i = (b * seqlen + t) * dim + d;
+                const long j = (b * seqlen + t) * dstate;
+                const double dt = oracle_softplus(delta[i] + bias_d);
+                double y = 0.0;
+                for (long n = 0; n < dstate; ++n) {
+                    const double B_tn = B[j + n];
+                    const double abar = exp(dt * A[n]);
+                    const double bbar = oracle_bbar(dt, A[n], B_tn, variant);
+                    hs[(t + 1) * dstate + n] = abar * hs[t * dstate + n] + bbar * u[i];
+                    y += C[j + n] * hs[(t + 1) * dstate + n];
+                }
+                if (D)
+                    y += D[d] * u[i];
+                dts[t] = dt;
+                ys[t] = y;
+            }
+            /* reverse */
+            for (long n = 0; n < dstate; ++n) {
+                hbar[n] = dlast ? dlast[(b * dim + d) * dstate + n] : 0.0;
+                Abar_acc[n] = 0.0;
+            }
+            for (long t = seqlen - 1; t >= 0; --t) {
+                const long i = (b * seqlen + t) * dim + d;
+                const long j = (b * seqlen + t) * dstate;
+                const double dt = dts[t];
+                /* out = y * SiLU(z) */
+                double ybar = dout[i];
+                if (z) {
+                    const double sg = oracle_sigmoid(z[i]);
+                    if (dz)
+                        dz[i] = dout[i] * ys[t] * sg * (1.0 + z[i] * (1.0 - sg));
+                    ybar = dout[i] * oracle_silu(z[i]);
+                } else if (dz) {
+                    dz[i] = 0.0;
+                }
+                /* y = sum_n C_n h_n + D u */
+                double ubar = 0.0;
+                if (D) {
+                    ubar += ybar * D[d];
+                    if (dD)
+                        dD[d] += ybar * u[i];
+                }
+                double dtbar = 0.0;
+                for (long n = 0; n < dstate; ++n) {
+                    const double h_t = hs[(t + 1) * dstate + n];
+                    const double h_prev = hs[t * dstate + n];
+                    dC[j + n] += ybar * h_t;
+                    hbar[n] += ybar * C[j + n];
+                    /* h_t = abar h_prev + bbar u */
+                    const double B_tn = B[j + n];
+                    const double abar = exp(dt * A[n]);
+                    const double bbar = oracle_bbar(dt, A[n], B_tn, variant);
+                    const double abar_bar = hbar[n] * h_prev;
+                    const double bbar_bar = hbar[n] * u[i];
+                    ubar += hbar[n] * bbar;
+                    /* abar = exp(dt A) */
+                    dtbar += abar_bar * abar * A[n];
+                    Abar_acc[n] += abar_bar * abar * dt;
+                    /* bbar */
+                    dB[j + n] += bbar_bar * oracle_bbar(dt, A[n], 1.0, variant); /* bbar is linear in B */
+                    if (variant == 1) {
+                        dtbar += bbar_bar * B_tn;
+                    } else {
+                        dtbar += bbar_bar * abar * B_tn;
+                        Abar_acc[n] += bbar_bar * B_tn * dt * dt * oracle_dphi(dt * A[n]);
+                    }
+                    hbar[n] *= abar; /* to h_prev */
+                }
+                /* dt = softplus(delta + bias) */
+                const double xbar = dtbar * oracle_sigmoid(delta[i] + bias_d);
+                ddelta[i] = xbar;
+                if (ddelta_bias)
+                    ddelta_bias[d] += xbar;
+                du[i] = ubar;
+            }
+            for (long n = 0; n < dstate; ++n) {
+                dA_log[d * dstate + n] += Abar_acc[n] * A[n]; /* A = -exp(A_log) */
+                if (dh0)
+                    dh0[(b * dim + d) * dstate + n] = hbar[n];
+            }
+        }
+    }
+    free(hs);
+    free(dts);
+    free(ys);
     return ORACLE_OK;
 }

@@ -20,6 +20,8 @@ Sources (page titles and passages):
 """
 from __future__ import annotations
 
+import functools
+
 import numpy as np
 from scipy import integrate
 from scipy.special import expit
@@ -406,6 +408,185 @@ def pin_conv_causal_window(orc, seed=13):
     return 0.0 if np.array_equal(changed, expect) else 1.0
 
 
+# ------------------------------------------------------------- backward pins
+# The gradient oracle is tied to the forward definition by routes that do not
+# use its chain-rule formulas: symbolic differentiation by sympy, central
+# finite differences of the (separately pinned) forward oracle, and exact
+# homogeneity identities of the forward map.
+
+_GRAD_KEYS = (("u", "du"), ("delta", "ddelta"), ("A_log", "dA_log"), ("B", "dB"), ("C", "dC"),
+              ("D", "dD"), ("z", "dz"), ("delta_bias", "ddelta_bias"), ("h0", "dh0"))
+
+
+def _bwd_case(rng, batch, L, dim, N, dt_regime="ordinary", h0=True):
+    c = {"u": rng.standard_normal((batch, L, dim)),
+         "A_log": np.log(rng.uniform(0.5, 4.0, (dim, N))),
+         "B": rng.standard_normal((batch, L, N)), "C": rng.standard_normal((batch, L, N)),
+         "D": rng.standard_normal(dim), "z": rng.standard_normal((batch, L, dim)),
+         "delta_bias": 0.3 * rng.standard_normal(dim),
+         "h0": rng.standard_normal((batch, dim, N)) if h0 else None}
+    if dt_regime == "tiny":   # dt = softplus(delta + bias) near 1e-4
+        c["delta"] = -9.0 + 0.5 * rng.standard_normal((batch, L, dim)) - c["delta_bias"]
+    else:
+        c["delta"] = 0.7 * rng.standard_normal((batch, L, dim))
+    return c
+
+
+def _symbolic_grads(case, dout, dlast, variant):
+    """Gradients of sum(dout*out) + sum(dlast*last) by sympy differentiation of the
+    forward written out symbolically (pages' definition), evaluated at 40 digits."""
+    import sympy as sp
+    batch, L, dim = case["u"].shape
+    N = case["A_log"].shape[1]
+    syms, vals = {}, []
+
+    def sym(name, idx, value):
+        s = sp.Symbol(f"{name}_{'_'.join(map(str, idx))}")
+        syms[(name, idx)] = s
+        vals.append(value)
+        return s
+
+    loss = 0
+    for b in range(batch):
+        for d in range(dim):
+            A = [-sp.exp(sym("A_log", (d, n), case["A_log"][d, n])) if b == 0 else
+                 -sp.exp(syms[("A_log", (d, n))]) for n in range(N)]
+            bias = sym("delta_bias", (d,), case["delta_bias"][d]) if b == 0 else syms[("delta_bias", (d,))]
+            Dd = sym("D", (d,), case["D"][d]) if b == 0 else syms[("D", (d,))]
+            h = [sym("h0", (b, d, n), case["h0"][b, d, n]) if case["h0"] is not None else sp.Integer(0)
+                 for n in range(N)]
+            for t in range(L):
+                u = sym("u", (b, t, d), case["u"][b, t, d])
+                x = sym("delta", (b, t, d), case["delta"][b, t, d]) + bias
+                dt = sp.log(1 + sp.exp(x))
+                y = 0
+                for n in range(N):
+                    Bs = sym("B", (b, t, n), case["B"][b, t, n]) if d == 0 else syms[("B", (b, t, n))]
+                    Cs = sym("C", (b, t, n), case["C"][b, t, n]) if d == 0 else syms[("C", (b, t, n))]
+                    bbar = dt * Bs if variant == 1 else (sp.exp(dt * A[n]) - 1) / A[n] * Bs
+                    h[n] = sp.exp(dt * A[n]) * h[n] + bbar * u
+                    y = y + Cs * h[n]
+                y = y + Dd * u
+                zs = sym("z", (b, t, d), case["z"][b, t, d])
+                loss = loss + dout[b, t, d] * y * zs / (1 + sp.exp(-zs))
+            for n in range(N):
+                loss = loss + dlast[b, d, n] * h[n]
+    keys = list(syms)
+    args = [syms[k] for k in keys]
+    grads = {}
+    for k in keys:
+        f = sp.lambdify(args, sp.diff(loss, syms[k]), modules="mpmath")
+        import mpmath
+        with mpmath.workdps(40):
+            grads[k] = float(f(*[mpmath.mpf(float(v)) for v in vals]))
+    return grads
+
+
+@functools.lru_cache(maxsize=None)
+def _symbolic_case(seed, variant, regime):
+    """The case and its sympy gradients; they depend on no oracle, so each is built once."""
+    rng = np.random.default_rng(seed)
+    case = _bwd_case(rng, 1, 3, 2, 2, dt_regime=regime, h0=regime != "tiny")
+    dout = rng.standard_normal(case["u"].shape)
+    dlast = rng.standard_normal((1, 2, 2))
+    return case, dout, dlast, _symbolic_grads(case, dout, dlast, variant)
+
+
+def _pin_bwd_symbolic(orc, seed, variant, regime):
+    case, dout, dlast, ref = _symbolic_case(seed, variant, regime)
+    g = orc.selective_scan_bwd(case["u"], case["delta"], case["A_log"], case["B"], case["C"], dout,
+                               D=case["D"], z=case["z"], delta_bias=case["delta_bias"], h0=case["h0"],
+                               dlast=dlast, variant=variant)
+    worst = 0.0
+    for name, key in _GRAD_KEYS:
+        if g[key] is None:
+            continue
+        r = np.zeros(g[key].shape)
+        for (nm, idx), v in ref.items():
+            if nm == name:
+                r[idx] = v
+        worst = max(worst, rel_err(g[key], r))
+    return worst
+
+
+def pin_bwd_symbolic_zoh(orc):
+    return _pin_bwd_symbolic(orc, 20, 0, "ordinary")
+
+
+def pin_bwd_symbolic_zoh_tiny_dt(orc):
+    return _pin_bwd_symbolic(orc, 21, 0, "tiny")
+
+
+def pin_bwd_symbolic_simplified(orc):
+    return _pin_bwd_symbolic(orc, 22, 1, "ordinary")
+
+
+def pin_bwd_finite_differences(orc, seed=23):
+    """Central differences of the forward oracle, every element of every input."""
+    rng = np.random.default_rng(seed)
+    case = _bwd_case(rng, 2, 6, 3, 4)
+    dout = rng.standard_normal(case["u"].shape)
+    dlast = rng.standard_normal(case["h0"].shape)
+    worst = 0.0
+    for variant in (0, 1):
+        g = orc.selective_scan_bwd(case["u"], case["delta"], case["A_log"], case["B"], case["C"], dout,
+                                   D=case["D"], z=case["z"], delta_bias=case["delta_bias"], h0=case["h0"],
+                                   dlast=dlast, variant=variant)
+
+        def loss(**kw):
+            a = dict(case)
+            a.update(kw)
+            out, last = orc.selective_scan(a["u"], a["delta"], a["A_log"], a["B"], a["C"], D=a["D"], z=a["z"],
+                                           delta_bias=a["delta_bias"], h0=a["h0"], variant=variant)
+            return float(np.sum(out * dout) + np.sum(last * dlast))
+
+        for name, key in _GRAD_KEYS:
+            arr = case[name]
+            fd = np.zeros(arr.shape)
+            for idx in np.ndindex(arr.shape):
+                e = 1e-5 * max(1.0, abs(arr[idx]))
+                p, m = arr.copy(), arr.copy()
+                p[idx] += e
+                m[idx] -= e
+                fd[idx] = (loss(**{name: p}) - loss(**{name: m})) / (2 * e)
+            worst = max(worst, rel_err(g[key], fd))
+    return worst
+
+
+def pin_bwd_homogeneity(orc, seed=24):
+    """Exact identities of the forward map, each a plain dot product:
+    out is linear in u (z absent): <dout, out> = <du, u>;
+    with D absent and h0 = 0, out is linear in B and in C: <dout, out> = <dB, B> = <dC, C>;
+    with u = 0, (out, last) is linear in h0: <dout, out> + <dlast, last> = <dh0, h0>."""
+    rng = np.random.default_rng(seed)
+    c = _bwd_case(rng, 2, 7, 3, 4)
+    dout = rng.standard_normal(c["u"].shape)
+    dlast = rng.standard_normal(c["h0"].shape)
+    errs = []
+    for variant in (0, 1):
+        out, _ = orc.selective_scan(c["u"], c["delta"], c["A_log"], c["B"], c["C"], D=c["D"],
+                                    delta_bias=c["delta_bias"], variant=variant)
+        g = orc.selective_scan_bwd(c["u"], c["delta"], c["A_log"], c["B"], c["C"], dout, D=c["D"],
+                                   delta_bias=c["delta_bias"], variant=variant)
+        lhs = np.sum(dout * out)
+        errs.append(abs(np.sum(g["du"] * c["u"]) - lhs) / abs(lhs))
+        out, _ = orc.selective_scan(c["u"], c["delta"], c["A_log"], c["B"], c["C"], z=c["z"],
+                                    delta_bias=c["delta_bias"], variant=variant)
+        g = orc.selective_scan_bwd(c["u"], c["delta"], c["A_log"], c["B"], c["C"], dout, z=c["z"],
+                                   delta_bias=c["delta_bias"], variant=variant)
+        lhs = np.sum(dout * out)
+        errs.append(abs(np.sum(g["dB"] * c["B"]) - lhs) / abs(lhs))
+        errs.append(abs(np.sum(g["dC"] * c["C"]) - lhs) / abs(lhs))
+        zero = np.zeros_like(c["u"])
+        out, last = orc.selective_scan(zero, c["delta"], c["A_log"], c["B"], c["C"], D=c["D"], z=c["z"],
+                                       delta_bias=c["delta_bias"], h0=c["h0"], variant=variant)
+        g = orc.selective_scan_bwd(zero, c["delta"], c["A_log"], c["B"], c["C"], dout, D=c["D"], z=c["z"],
+                                   delta_bias=c["delta_bias"], h0=c["h0"], dlast=dlast, variant=variant)
+        lhs = np.sum(dout * out) + np.sum(dlast * last)
+        errs.append(abs(np.sum(g["dh0"] * c["h0"]) - lhs) / abs(lhs))
+    return float(max(errs))
+
+
 # name -> (function, tolerance)
 PINS = {
     "zoh_matches_ode": (pin_zoh_matches_ode, 1e-10),
@@ -422,4 +603,9 @@ PINS = {
     "conv_identity_tap": (pin_conv_identity_tap, 1e-14),
     "conv_matches_numpy": (pin_conv_matches_numpy, 1e-12),
     "conv_causal_window": (pin_conv_causal_window, 0.0),
+    "bwd_symbolic_zoh": (pin_bwd_symbolic_zoh, 1e-12),
+    "bwd_symbolic_zoh_tiny_dt": (pin_bwd_symbolic_zoh_tiny_dt, 1e-12),
+    "bwd_symbolic_simplified": (pin_bwd_symbolic_simplified, 1e-12),
+    "bwd_finite_differences": (pin_bwd_finite_differences, 1e-7),
+    "bwd_homogeneity": (pin_bwd_homogeneity, 1e-12),
 }

@@ -44,6 +44,20 @@ MUTANTS = {
     # circular instead of causal zero padding (every index stays inside x)
     "conv_circular_padding": ("const long ts = t - (width - 1) + k;",
                               "const long ts = (t - (width - 1) + k + seqlen) % seqlen;"),
+    # backward
+    "bwd_dphi_series_coefficient": ("0.5 + s * (1.0 / 3.0 +", "0.5 + s * (1.0 / 4.0 +"),
+    "bwd_state_adjoint_not_decayed": ("hbar[n] *= abar; /* to h_prev */", "/* adjoint not carried */"),
+    "bwd_abar_adjoint_uses_h_t": ("const double abar_bar = hbar[n] * h_prev;",
+                                  "const double abar_bar = hbar[n] * h_t;"),
+    "bwd_silu_derivative_is_sigmoid": ("dout[i] * ys[t] * sg * (1.0 + z[i] * (1.0 - sg))", "dout[i] * ys[t] * sg"),
+    "bwd_softplus_derivative_sign": ("dtbar * oracle_sigmoid(delta[i] + bias_d)",
+                                     "dtbar * oracle_sigmoid(-(delta[i] + bias_d))"),
+    "bwd_A_log_chain_sign": ("Abar_acc[n] * A[n]; /* A = -exp(A_log) */", "Abar_acc[n] * -A[n];"),
+    "bwd_dt_through_bbar_dropped": ("dtbar += bbar_bar * abar * B_tn;", "dtbar += 0.0;"),
+    "bwd_D_path_to_u_dropped": ("ubar += ybar * D[d];", "ubar += 0.0;"),
+    "bwd_dC_uses_h_prev": ("dC[j + n] += ybar * h_t;", "dC[j + n] += ybar * h_prev;"),
+    "bwd_u_through_state_dropped": ("ubar += hbar[n] * bbar;", "ubar += 0.0 * bbar;"),
+    "bwd_readout_adjoint_dropped": ("hbar[n] += ybar * C[j + n];", "hbar[n] += 0.0 * C[j + n];"),
 }
 
 
