@@ -247,6 +247,54 @@ MAMBA_API mamba_status_t mamba_selective_state_update_ex(
     const void *B, const void *C, const float *D, const void *z,
     const float *delta_bias, void *out, int discretization, mamba_stream_t stream);
 
+/*
+ * Backward of the scan: the gradients of
+ *   loss = sum_{b,t,d} dout[b,t,d] * out[b,t,d] + sum_{b,d,n} dlast_state[b,d,n] * last_state[b,d,n]
+ * with respect to every input of mamba_selective_scan_fwd_ex, for the same
+ * forward ("State Space Models and Mamba" §2-§4: zero-order hold, or the
+ * simplified Bbar = dt B of the "Mamba" paper notes' selective_ssm sketch,
+ * chosen by `discretization`; D skip and SiLU gate as in the forward). The
+ * forward is recomputed from the inputs: the call needs no saved activations.
+ *
+ * Inputs (as for the forward; device pointers, row-major, contiguous):
+ *   u, delta, z (z may be NULL)      : (B, L, D) in_dtype
+ *   A_log                            : (D, N) fp32
+ *   B, C                             : (B, L, N) in_dtype
+ *   D, delta_bias                    : (D,) fp32 or NULL (= 0)
+ *   initial_state                    : (B, D, N) fp32 or NULL (= 0)
+ *   dout                             : (B, L, D) in_dtype, the gradient of out
+ *   dlast_state                      : (B, D, N) fp32 or NULL (= 0)
+ * Outputs (written; none is accumulated into):
+ *   du, ddelta                       : (B, L, D) in_dtype, required
+ *   dz                               : (B, L, D) in_dtype; must be NULL when z is NULL
+ *   dA_log                           : (D, N) fp32, required
+ *   dB, dC                           : (B, L, N) fp32, required
+ *   dD, ddelta_bias                  : (D,) fp32 or NULL (not computed); computed
+ *                                      even when D / delta_bias is NULL
+ *   dinitial_state                   : (B, D, N) fp32 or NULL (not computed)
+ * dstate must be 16, 32, 64 or 128 (MAMBA_ERR_UNSUPPORTED otherwise); batch
+ * <= 65535. The fp32 arrays read or written four at a time (initial_state,
+ * dlast_state, dA_log, dB, dC, dinitial_state) must be 16-byte aligned
+ * (MAMBA_ERR_UNSUPPORTED otherwise). Outputs may not alias inputs or each
+ * other (MAMBA_ERR_INVALID_ARG).
+ *
+ * Work: the call zeroes dA_log, dB, dC, dD, ddelta_bias on `stream`, then one
+ * kernel launch runs the forward over each channel, stores the state every 16
+ * steps in a stream-ordered workspace of B * ceil(L/16) * D * N * 4 bytes
+ * (cudaMallocAsync / cudaFreeAsync on `stream`), and walks the chunks
+ * backwards. dB, dC, dA_log, dD and ddelta_bias are sums over channels or
+ * batch rows taken with fp32 atomics, so their last bits may differ from call
+ * to call. MAMBA_F32 inputs use expf / expm1f; MAMBA_BF16 inputs use the
+ * hardware ex2 / rcp approximations, as the forward does.
+ */
+MAMBA_API mamba_status_t mamba_selective_scan_bwd(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, int discretization,
+    const void *u, const void *delta, const float *A_log, const void *B, const void *C,
+    const float *D, const void *z, const float *delta_bias, const float *initial_state,
+    const void *dout, const float *dlast_state,
+    void *du, void *ddelta, float *dA_log, float *dB, float *dC,
+    float *dD, void *dz, float *ddelta_bias, float *dinitial_state, mamba_stream_t stream);
+
 /* Static description of a status code. */
 MAMBA_API const char *mamba_status_string(mamba_status_t s);
 

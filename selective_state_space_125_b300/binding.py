@@ -28,7 +28,8 @@ EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_selective_state_update", "mamba_status_string",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
             "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc",
-            "mamba_selective_state_update_ex", "mamba_conv1d_selective_scan_fwd")
+            "mamba_selective_state_update_ex", "mamba_conv1d_selective_scan_fwd",
+            "mamba_selective_scan_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def library() -> ctypes.CDLL:
             lib.mamba_conv1d_selective_scan_fwd.argtypes = ([i, i, i, i, i] + [vp] * 3 + [i] + [vp] * 10 +
                                                             [ctypes.POINTER(ScanPlan), vp])
             lib.mamba_conv1d_selective_scan_fwd.restype = i
+            lib.mamba_selective_scan_bwd.argtypes = [i, i, i, i, i, i] + [vp] * 20 + [vp]
+            lib.mamba_selective_scan_bwd.restype = i
             lib.mamba_status_string.argtypes = [i]
             lib.mamba_status_string.restype = ctypes.c_char_p
             lib.mamba_last_error_detail.argtypes = []
@@ -179,6 +182,52 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
     if last_state is not None:
         return out, last_state
     return out
+
+
+def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
+                             initial_state=None, dlast_state=None, *, discretization=MAMBA_ZOH,
+                             need_dD=None, need_ddelta_bias=None, need_dinitial_state=None, stream=None):
+    """Gradients of sum(dout * out) + sum(dlast_state * last_state) through the C ABI.
+
+    Inputs as for ``mamba_selective_scan_fwd``; dout is like u and dlast_state
+    (batch, dim, N) float32 or None. Returns a dict with du, ddelta (like u), dz
+    (like u, or None without z), dA_log (dim, N), dB, dC (batch, L, N) float32,
+    and dD, ddelta_bias (dim,), dinitial_state (batch, dim, N) float32 -- each
+    computed when the matching input is given or its ``need_*`` flag is set,
+    else None.
+    """
+    torch = _torch()
+    batch, seqlen, dim = u.shape
+    dstate = A_log.shape[1]
+    dev = u.device
+    code = _dtype_code(u)
+    xs = (batch, seqlen, dim)
+    bcs = (batch, seqlen, dstate)
+    f32 = dict(dtype=torch.float32, device=dev)
+    want = lambda flag, given: given if flag is None else bool(flag)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dz": torch.empty_like(u) if z is not None else None,
+         "dA_log": torch.empty((dim, dstate), **f32),
+         "dB": torch.empty(bcs, **f32), "dC": torch.empty(bcs, **f32),
+         "dD": torch.empty((dim,), **f32) if want(need_dD, D is not None) else None,
+         "ddelta_bias": torch.empty((dim,), **f32) if want(need_ddelta_bias, delta_bias is not None) else None,
+         "dinitial_state": (torch.empty((batch, dim, dstate), **f32)
+                            if want(need_dinitial_state, initial_state is not None) else None)}
+    st = (batch, dim, dstate)
+    check(library().mamba_selective_scan_bwd(
+        batch, dim, dstate, seqlen, code, int(discretization),
+        _ptr(u, "u", xs, u.dtype, dev), _ptr(delta, "delta", xs, u.dtype, dev),
+        _ptr(A_log, "A_log", (dim, dstate), torch.float32, dev),
+        _ptr(B, "B", bcs, u.dtype, dev), _ptr(C, "C", bcs, u.dtype, dev),
+        _ptr(D, "D", (dim,), torch.float32, dev), _ptr(z, "z", xs, u.dtype, dev),
+        _ptr(delta_bias, "delta_bias", (dim,), torch.float32, dev),
+        _ptr(initial_state, "initial_state", st, torch.float32, dev),
+        _ptr(dout, "dout", xs, u.dtype, dev), _ptr(dlast_state, "dlast_state", st, torch.float32, dev),
+        _ptr(g["du"], "du"), _ptr(g["ddelta"], "ddelta"), _ptr(g["dA_log"], "dA_log"),
+        _ptr(g["dB"], "dB"), _ptr(g["dC"], "dC"), _ptr(g["dD"], "dD"), _ptr(g["dz"], "dz"),
+        _ptr(g["ddelta_bias"], "ddelta_bias"), _ptr(g["dinitial_state"], "dinitial_state"),
+        _stream(stream, dev)))
+    return g
 
 
 def mamba_conv1d_selective_scan_fwd(x, conv_weight, conv_bias, delta, A_log, B, C, D=None, z=None,

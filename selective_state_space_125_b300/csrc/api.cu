@@ -14,6 +14,7 @@
 #include <string>
 
 #include "mamba_ssm.h"
+#include "bwd_args.h"
 #include "decode_args.h"
 #include "scan_args.h"
 
@@ -489,6 +490,122 @@ mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamb
                                             void* out, mamba_stream_t stream) {
   return mamba_selective_state_update_ex(batch, dim, dstate, in_dtype, state, u, delta, A_log, B, C, D, z,
                                          delta_bias, out, 0, stream);
+}
+
+mamba_status_t mamba_selective_scan_bwd(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                        int discretization, const void* u, const void* delta, const float* A_log,
+                                        const void* B, const void* C, const float* D, const void* z,
+                                        const float* delta_bias, const float* initial_state, const void* dout,
+                                        const float* dlast_state, void* du, void* ddelta, float* dA_log, float* dB,
+                                        float* dC, float* dD, void* dz, float* ddelta_bias, float* dinitial_state,
+                                        mamba_stream_t stream_) {
+  t_detail.clear();
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (batch < 0 || dim < 0 || seqlen < 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
+  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
+  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
+  if (discretization < 0 || discretization > 1)
+    return fail(MAMBA_ERR_INVALID_ARG, "unknown discretization %d", discretization);
+  if (!scan_bwd_supported(dstate))
+    return fail(MAMBA_ERR_UNSUPPORTED, "the backward scan is built for dstate 16, 32, 64 or 128 (got %d)", dstate);
+  if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
+  if (!z && dz) return fail(MAMBA_ERR_INVALID_ARG, "dz given without z");
+  if (dim > 0 && (!A_log || !dA_log)) return fail(MAMBA_ERR_INVALID_ARG, "A_log and dA_log are required");
+  const bool work = batch > 0 && dim > 0 && seqlen > 0;
+  if (work && (!u || !delta || !B || !C || !dout || !du || !ddelta || !dB || !dC))
+    return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL");
+  const float* f4[] = {initial_state, dlast_state, dA_log, dB, dC, dinitial_state};
+  for (const float* p : f4)
+    if (p && !aligned16(p))
+      return fail(MAMBA_ERR_UNSUPPORTED, "fp32 state / gradient arrays must be 16-byte aligned (%p)", (const void*)p);
+
+  const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
+  const size_t es = dtype == 0 ? 4 : 2;
+  const size_t nx = (size_t)batch * seqlen * dim * es;
+  const size_t nbc = (size_t)batch * seqlen * dstate * es;
+  const size_t nbc32 = (size_t)batch * seqlen * dstate * 4;
+  const size_t ns = (size_t)batch * dim * dstate * 4;
+  const size_t np = (size_t)dim * dstate * 4, nd = (size_t)dim * 4;
+  const void* ins[] = {u, delta, A_log, B, C, D, z, delta_bias, initial_state, dout, dlast_state};
+  const size_t in_sz[] = {nx, nx, np, nbc, nbc, nd, nx, nd, ns, nx, ns};
+  void* outs[] = {du, ddelta, dA_log, dB, dC, dD, dz, ddelta_bias, dinitial_state};
+  const size_t out_sz[] = {nx, nx, np, nbc32, nbc32, nd, nx, nd, ns};
+  for (int i = 0; i < 9; ++i) {
+    for (int j = 0; j < 11; ++j)
+      if (overlaps(outs[i], out_sz[i], ins[j], in_sz[j]))
+        return fail(MAMBA_ERR_INVALID_ARG, "output %d aliases input %d", i, j);
+    for (int j = 0; j < i; ++j)
+      if (overlaps(outs[i], out_sz[i], outs[j], out_sz[j]))
+        return fail(MAMBA_ERR_INVALID_ARG, "output %d aliases output %d", i, j);
+  }
+
+  // Sums start from zero.
+  cudaError_t e = cudaSuccess;
+  if (dim > 0) e = cudaMemsetAsync(dA_log, 0, np, stream);
+  if (e == cudaSuccess && dD && dim > 0) e = cudaMemsetAsync(dD, 0, nd, stream);
+  if (e == cudaSuccess && ddelta_bias && dim > 0) e = cudaMemsetAsync(ddelta_bias, 0, nd, stream);
+  if (e == cudaSuccess && nbc32 > 0) e = cudaMemsetAsync(dB, 0, nbc32, stream);
+  if (e == cudaSuccess && nbc32 > 0) e = cudaMemsetAsync(dC, 0, nbc32, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "zeroing the gradient sums");
+  if (batch == 0 || dim == 0) return MAMBA_OK;
+  if (seqlen == 0) {  // last_state = initial_state
+    if (dinitial_state) {
+      e = dlast_state ? cudaMemcpyAsync(dinitial_state, dlast_state, ns, cudaMemcpyDeviceToDevice, stream)
+                      : cudaMemsetAsync(dinitial_state, 0, ns, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "empty-sequence dinitial_state");
+    }
+    return MAMBA_OK;
+  }
+
+  // 16-byte slots when every (B, L, D) / (B, L, N) tensor allows them.
+  const int cb = kBwdThreads / (dstate / 4);
+  const size_t sbx = std::min<size_t>(16, (size_t)cb * es);
+  bool aligned = ((size_t)dim * es) % sbx == 0;
+  const void* xs[] = {u, delta, z, dout, du, ddelta, dz, B, C};
+  for (const void* p : xs)
+    if (p && !aligned16(p)) aligned = false;
+
+  BwdArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.batch = batch;
+  a.dim = dim;
+  a.dstate = dstate;
+  a.seqlen = seqlen;
+  a.nchunk = (seqlen + kBwdChunk - 1) / kBwdChunk;
+  a.u = u;
+  a.delta = delta;
+  a.z = z;
+  a.B = B;
+  a.C = C;
+  a.dout = dout;
+  a.A_log = A_log;
+  a.D = D;
+  a.delta_bias = delta_bias;
+  a.h0 = initial_state;
+  a.dlast = dlast_state;
+  a.du = du;
+  a.ddelta = ddelta;
+  a.dz = dz;
+  a.dA_log = dA_log;
+  a.dB = dB;
+  a.dC = dC;
+  a.dD = dD;
+  a.ddelta_bias = ddelta_bias;
+  a.dh0 = dinitial_state;
+  a.disc = discretization;
+  a.aligned = aligned ? 1 : 0;
+  const size_t ck_bytes = (size_t)batch * a.nchunk * dim * dstate * sizeof(float);
+  void* ck = nullptr;
+  e = cudaMallocAsync(&ck, ck_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(backward checkpoint workspace)");
+  a.ck = static_cast<float*>(ck);
+  e = launch_scan_bwd(dtype, a, stream);
+  cudaError_t e2 = cudaFreeAsync(ck, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward scan launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync(backward checkpoint workspace)");
+  return MAMBA_OK;
 }
 
 const char* mamba_status_string(mamba_status_t s) {

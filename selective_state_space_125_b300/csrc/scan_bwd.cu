@@ -1,0 +1,492 @@
+// Backward of the selective scan: the gradients of
+//   loss = sum_{b,t,d} dout * out + sum_{b,d,n} dlast * last_state
+// with respect to u, delta, A_log, B, C, D, z, delta_bias and the initial
+// state, for the recurrence of "State Space Models and Mamba" §2-§4 (zero-order
+// hold, or the simplified Bbar = dt B) with the D skip and SiLU gate of the
+// "Mamba" paper notes (selective_ssm sketch, Overall framework).
+//
+// Work layout: a CTA owns CB channels of one batch row; LPC = N / 4 threads
+// share a channel, 4 states each. Phase 1 runs the forward recurrence over the
+// sequence and writes the state at the start of every 16-step chunk to a
+// workspace; each thread reads back only the slots it wrote. Phase 2 walks the
+// chunks backwards. For each chunk it stages the tiles (u, delta, z, dout, B,
+// C) in shared memory, recomputes the chunk's states from its checkpoint into
+// a per-thread shared-memory history, and runs the adjoint recurrence
+//   lambda_t = dy_t C_t + abar_{t+1} lambda_{t+1}    (lambda = dloss / dh_t)
+// backwards through the chunk. The tiles of the next chunk are loaded into
+// registers while the current one is computed.
+//
+// Per step and state, with abar = exp(dt A), q = (abar - 1) / A (zero-order
+// hold) or dt (simplified), and v = A h_{t-1} + B u:
+//   dloss/d dt    += abar lambda v                    (simplified: lambda (abar A h_{t-1} + B u))
+//   dloss/d A_log += dt abar lambda v - q lambda B u   (simplified: dt abar lambda A h_{t-1})
+//   dloss/d B_n   += lambda q u,   dloss/d u += lambda q B_n,   dloss/d C_n += dy h_t
+// (dA_log = A dA because A = -exp(A_log).) The sums over states of the dt and
+// u terms are reduced across the LPC threads of a channel with shuffles; the
+// sums of dB and dC over channels are reduce-scattered across the channels of
+// a warp, added across warps in shared memory and once per chunk into global
+// memory. Per-channel sums over the batch (dA_log, dD, ddelta_bias) are added
+// with one atomic per thread at the end.
+//
+// Math: bf16 inputs use MUFU ex2/rcp and keep the scaled state s = A h during
+// the recomputation (s_t = abar (s_{t-1} + B u) - B u, so A h_{t-1} is read
+// directly); fp32 inputs use expm1f and the unscaled h, as the forward does.
+#include <type_traits>
+
+#include "bwd_args.h"
+#include "device_common.cuh"
+
+namespace mamba {
+namespace {
+
+template <int SB> struct RawOf;
+template <> struct RawOf<16> { using type = uint4; };
+template <> struct RawOf<8> { using type = uint2; };
+template <> struct RawOf<4> { using type = unsigned int; };
+template <> struct RawOf<2> { using type = unsigned short; };
+
+constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return hw_rcp(1.0f + hw_ex2(-x * kLog2e)); }
+__device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+template <typename Tin, int N, bool ALIGNED>
+struct BwdGeom {
+  static constexpr int NPL = 4;
+  static constexpr int LPC = N / NPL;
+  static constexpr int CB = kBwdThreads / LPC;
+  static constexpr int K = kBwdChunk;
+  static constexpr int ES = int(sizeof(Tin));
+  static constexpr int SBX = ALIGNED ? (CB * ES < 16 ? CB * ES : 16) : ES;  // bytes per slot of a (t, d) tile
+  static constexpr int SBB = ALIGNED ? 16 : ES;                             // bytes per slot of a (t, n) tile
+  static constexpr size_t szX = size_t(K) * CB * ES;
+  static constexpr size_t szBC = size_t(K) * N * ES;
+  static constexpr size_t szF = size_t(K) * CB * 4;
+  static constexpr size_t oX = 0;                                      // raw u, delta, z, dout tiles
+  static constexpr size_t oBC = align16(oX + 4 * szX);                 // raw B, C tiles
+  static constexpr size_t oO = align16(oBC + 2 * szBC);                // raw du, ddelta, dz tiles
+  static constexpr size_t oF = align16(oO + 3 * szX);                  // dt, sigmoid, dy, dz factor, u
+  static constexpr size_t oBf = oF + 5 * szF;                          // B, C as float
+  static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [K][2N] dB | dC of the chunk
+  static constexpr size_t oCh = oAcc + size_t(K) * 2 * N * 4;          // per-channel bias, D
+  static constexpr size_t oHist = align16(oCh + 2 * size_t(CB) * 4);   // [K+1][threads] states
+  static constexpr size_t kSmem = oHist + size_t(K + 1) * kBwdThreads * 16;
+  static_assert(N % 16 == 0 && LPC <= 32, "state size must be 16, 32, 64 or 128");
+  static_assert((CB * ES) % SBX == 0 && (N * ES) % SBB == 0, "slot width must divide a tile row");
+};
+
+// Copies of NT tiles of [K][W] elements between global memory and shared
+// memory in SB-byte slots. The slot space is tile-major, so slot s sits at
+// byte s * SB of the shared-memory tile area (each tile K * W * ES bytes).
+// Element (row, e) of tile `tile` is at base(tile) + (row0 + row) * stride +
+// col0 + e in global memory; rows >= nrows, columns >= ncols and null bases
+// are skipped (zero on load).
+template <int ES, int SB, int W, int K, int NT>
+struct TileCopy {
+  static constexpr int kRow = W * ES / SB;
+  static constexpr int kTile = K * kRow;
+  static constexpr int kTotal = NT * kTile;
+  static constexpr int kPer = (kTotal + kBwdThreads - 1) / kBwdThreads;
+  using Raw = typename RawOf<SB>::type;
+  Raw r[kPer];
+
+  template <class Src>
+  __device__ __forceinline__ void load(Src src, size_t row0, size_t stride, int col0, int ncols, int nrows,
+                                       int tid) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int s = tid + j * kBwdThreads;
+      r[j] = Raw{};
+      if (s < kTotal) {
+        const int tile = s / kTile, rem = s - tile * kTile, row = rem / kRow, e = (rem - row * kRow) * (SB / ES);
+        const unsigned char* base = static_cast<const unsigned char*>(src(tile));
+        if (base != nullptr && row < nrows && e < ncols)
+          r[j] = *reinterpret_cast<const Raw*>(base + ((row0 + row) * stride + col0 + e) * ES);
+      }
+    }
+  }
+  __device__ __forceinline__ void to_smem(unsigned char* dst, int tid) const {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int s = tid + j * kBwdThreads;
+      if (s < kTotal) *reinterpret_cast<Raw*>(dst + size_t(s) * SB) = r[j];
+    }
+  }
+  template <class Dst>
+  static __device__ __forceinline__ void smem_to_global(const unsigned char* srcsm, Dst dst, size_t row0,
+                                                        size_t stride, int col0, int ncols, int nrows, int tid) {
+    for (int s = tid; s < kTotal; s += kBwdThreads) {
+      const int tile = s / kTile, rem = s - tile * kTile, row = rem / kRow, e = (rem - row * kRow) * (SB / ES);
+      unsigned char* base = static_cast<unsigned char*>(dst(tile));
+      if (base != nullptr && row < nrows && e < ncols)
+        *reinterpret_cast<Raw*>(base + ((row0 + row) * stride + col0 + e) * ES) =
+            *reinterpret_cast<const Raw*>(srcsm + size_t(s) * SB);
+    }
+  }
+};
+
+// One round of a reduce-scatter across the lanes that differ in bit `m`: each
+// lane keeps half of its M values (the upper half if its bit is set), summed
+// with the partner's copy of that half.
+template <int M>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane, int m) {
+  const bool up = (lane & m) != 0;
+#pragma unroll
+  for (int i = 0; i < M / 2; ++i) {
+    const float send = up ? v[i] : v[i + M / 2];
+    const float keep = up ? v[i + M / 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+  }
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
+template <typename Tin, int N, int DISC, bool ALIGNED>
+__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) {
+  using G = BwdGeom<Tin, N, ALIGNED>;
+  using E = Elem<Tin>;
+  constexpr bool PRECISE = std::is_same<Tin, float>::value;
+  constexpr int K = G::K, CB = G::CB, LPC = G::LPC, NPL = G::NPL, ES = G::ES;
+  using XCopy2 = TileCopy<ES, G::SBX, CB, K, 2>;  // u, delta
+  using XCopy4 = TileCopy<ES, G::SBX, CB, K, 4>;  // u, delta, z, dout
+  using OCopy3 = TileCopy<ES, G::SBX, CB, K, 3>;  // du, ddelta, dz
+  using BCopy1 = TileCopy<ES, G::SBB, N, K, 1>;   // B
+  using BCopy2 = TileCopy<ES, G::SBB, N, K, 2>;   // B, C
+
+  extern __shared__ __align__(16) unsigned char sm[];
+  const Tin* xs = reinterpret_cast<const Tin*>(sm + G::oX);
+  const Tin* bs = reinterpret_cast<const Tin*>(sm + G::oBC);
+  Tin* os = reinterpret_cast<Tin*>(sm + G::oO);
+  float* f_dt = reinterpret_cast<float*>(sm + G::oF);
+  float* f_sg = f_dt + K * CB;
+  float* f_dy = f_sg + K * CB;
+  float* f_dz = f_dy + K * CB;
+  float* f_u = f_dz + K * CB;
+  float* f_B = reinterpret_cast<float*>(sm + G::oBf);
+  float* f_C = f_B + K * N;
+  float* acc = reinterpret_cast<float*>(sm + G::oAcc);
+  float* ch_bias = reinterpret_cast<float*>(sm + G::oCh);
+  float* ch_D = ch_bias + CB;
+  float4* hist = reinterpret_cast<float4*>(sm + G::oHist);
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c = tid / LPC, part = tid % LPC, n0 = part * NPL;
+  const int b = blockIdx.y;
+  const int Dm = a.dim, L = a.seqlen, nck = a.nchunk;
+  const int d0 = blockIdx.x * CB;
+  const int nch = min(CB, Dm - d0);
+  const int d = d0 + c;
+  const bool cv = c < nch;
+  const bool has_z = a.z != nullptr;
+  const size_t rowb = (size_t)b * L;
+  // checkpoint slot of chunk ci: ck[((b * nck + ci) * D + d) * N + n0]
+  float* ckp = a.ck + ((size_t)b * nck * Dm + (cv ? d : 0)) * N + n0;
+  const size_t ck_stride = (size_t)Dm * N;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (tid < CB) {
+    const bool ok = tid < nch;
+    ch_bias[tid] = (ok && a.delta_bias) ? a.delta_bias[d0 + tid] : 0.0f;
+    ch_D[tid] = (ok && a.D) ? a.D[d0 + tid] : 0.0f;
+  }
+  for (int i = tid; i < K * 2 * N; i += kBwdThreads) acc[i] = 0.0f;
+
+  // A = -exp(A_log), 1/A and (fast path) A log2(e) for my states.
+  float A[NPL], Al[NPL], Ik[NPL];
+#pragma unroll
+  for (int k = 0; k < NPL; ++k) {
+    const float al = cv ? a.A_log[(size_t)d * N + n0 + k] : 0.0f;
+    if constexpr (PRECISE) {
+      A[k] = -expf(al);
+      Ik[k] = 1.0f / A[k];
+      Al[k] = A[k];
+    } else {
+      A[k] = -hw_ex2(al * kLog2e);
+      Ik[k] = hw_rcp(A[k]);
+      Al[k] = A[k] * kLog2e;
+    }
+  }
+
+  // ------------------------------------------------ phase 1: checkpoints
+  float s[NPL];  // h (fp32 inputs) or A h (bf16 inputs)
+  {
+    const float4 h = (cv && a.h0) ? ld4(a.h0 + ((size_t)b * Dm + d) * N + n0) : zero4;
+    s[0] = h.x; s[1] = h.y; s[2] = h.z; s[3] = h.w;
+    if constexpr (!PRECISE) {
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) s[k] *= A[k];
+    }
+  }
+  {
+    XCopy2 xp;
+    BCopy1 bp;
+    auto src_x = [&](int tile) -> const void* { return tile == 0 ? a.u : a.delta; };
+    auto src_b = [&](int) -> const void* { return a.B; };
+    if (nck > 1) {
+      xp.load(src_x, rowb, Dm, d0, nch, K, tid);
+      bp.load(src_b, rowb, N, 0, N, K, tid);
+    }
+    for (int ci = 0; ci < nck; ++ci) {
+      if (cv) {
+        float4 h;
+        if constexpr (PRECISE) h = make_float4(s[0], s[1], s[2], s[3]);
+        else h = make_float4(s[0] * Ik[0], s[1] * Ik[1], s[2] * Ik[2], s[3] * Ik[3]);
+        st4(ckp + ci * ck_stride, h);
+      }
+      if (ci == nck - 1) break;  // the last chunk's end state is not needed
+      __syncthreads();
+      xp.to_smem(sm + G::oX, tid);
+      bp.to_smem(sm + G::oBC, tid);
+      __syncthreads();
+      if (ci + 2 < nck) {  // chunks before the last one are full
+        xp.load(src_x, rowb + (ci + 1) * K, Dm, d0, nch, K, tid);
+        bp.load(src_b, rowb + (ci + 1) * K, N, 0, N, K, tid);
+      }
+      for (int p = tid; p < K * CB; p += kBwdThreads) {
+        const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
+        f_dt[p] = PRECISE ? softplus_precise(x) : softplus_fast(x);
+        f_u[p] = E::load(xs + p);
+      }
+      for (int p = tid; p < K * N; p += kBwdThreads) f_B[p] = E::load(bs + p);
+      __syncthreads();
+#pragma unroll 4
+      for (int t = 0; t < K; ++t) {
+        const float dt = f_dt[t * CB + c], uu = f_u[t * CB + c];
+        const float4 B4 = ld4(f_B + t * N + n0);
+        const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+          const float Bu = Bv[k] * uu;
+          if constexpr (PRECISE) {
+            const float e = expm1f(dt * A[k]);
+            const float q = DISC ? dt : e * Ik[k];
+            s[k] = fmaf(e, s[k], fmaf(q, Bu, s[k]));  // h <- (1 + e) h + q B u
+          } else {
+            const float ab = hw_ex2(dt * Al[k]);
+            if (DISC == 0) s[k] = fmaf(ab, s[k] + Bu, -Bu);  // s <- abar (s + B u) - B u
+            else s[k] = fmaf(ab, s[k], A[k] * dt * Bu);      // s <- abar s + A dt B u
+          }
+        }
+      }
+    }
+  }
+
+  // --------------------------------------------------- phase 2: adjoint
+  float carry[NPL];  // abar_{t+1} lambda_{t+1} (dlast before the last step)
+  {
+    const float4 g = (cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
+    carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
+  }
+  float dAl[NPL] = {0.f, 0.f, 0.f, 0.f};
+  float dD_acc = 0.0f, dbias_acc = 0.0f;
+  XCopy4 xq;
+  BCopy2 bq;
+  auto src_x4 = [&](int tile) -> const void* {
+    return tile == 0 ? a.u : (tile == 1 ? a.delta : (tile == 2 ? a.z : a.dout));
+  };
+  auto src_bc = [&](int tile) -> const void* { return tile == 0 ? a.B : a.C; };
+  auto dst_o = [&](int tile) -> void* { return tile == 0 ? a.du : (tile == 1 ? a.ddelta : a.dz); };
+  float4 ckn;
+  {
+    const int t0 = (nck - 1) * K;
+    xq.load(src_x4, rowb + t0, Dm, d0, nch, L - t0, tid);
+    bq.load(src_bc, rowb + t0, N, 0, N, L - t0, tid);
+    ckn = cv ? ld4(ckp + (nck - 1) * ck_stride) : zero4;
+  }
+  for (int ci = nck - 1; ci >= 0; --ci) {
+    const int t0 = ci * K, tv = min(K, L - t0);
+    __syncthreads();
+    xq.to_smem(sm + G::oX, tid);
+    bq.to_smem(sm + G::oBC, tid);
+    const float4 cks = ckn;
+    __syncthreads();
+    if (ci > 0) {
+      xq.load(src_x4, rowb + t0 - K, Dm, d0, nch, K, tid);
+      bq.load(src_bc, rowb + t0 - K, N, 0, N, K, tid);
+      ckn = cv ? ld4(ckp + (ci - 1) * ck_stride) : zero4;
+    }
+    for (int p = tid; p < K * CB; p += kBwdThreads) {
+      const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
+      const float g = E::load(xs + 3 * K * CB + p);
+      f_u[p] = E::load(xs + p);
+      f_dt[p] = PRECISE ? softplus_precise(x) : softplus_fast(x);
+      f_sg[p] = PRECISE ? sigmoid_precise(x) : sigmoid_fast(x);
+      if (has_z) {
+        const float zz = E::load(xs + 2 * K * CB + p);
+        const float sz = PRECISE ? sigmoid_precise(zz) : sigmoid_fast(zz);
+        f_dy[p] = g * zz * sz;                           // dloss/dy = dout SiLU(z)
+        f_dz[p] = g * sz * fmaf(zz, 1.0f - sz, 1.0f);  // dloss/dz = y * this
+      } else {
+        f_dy[p] = g;
+        f_dz[p] = 0.0f;
+      }
+    }
+    for (int p = tid; p < K * N; p += kBwdThreads) {
+      f_B[p] = E::load(bs + p);
+      f_C[p] = E::load(bs + K * N + p);
+    }
+    __syncthreads();
+
+    // recompute the chunk's states: hist[t + 1] = state after step t0 + t
+    float st[NPL] = {cks.x, cks.y, cks.z, cks.w};
+    if constexpr (!PRECISE) {
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) st[k] *= A[k];
+    }
+    hist[tid] = make_float4(st[0], st[1], st[2], st[3]);
+#pragma unroll 4
+    for (int t = 0; t < tv; ++t) {
+      const float dt = f_dt[t * CB + c], uu = f_u[t * CB + c];
+      const float4 B4 = ld4(f_B + t * N + n0);
+      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        const float Bu = Bv[k] * uu;
+        if constexpr (PRECISE) {
+          const float e = expm1f(dt * A[k]);
+          const float q = DISC ? dt : e * Ik[k];
+          st[k] = fmaf(e, st[k], fmaf(q, Bu, st[k]));
+        } else {
+          const float ab = hw_ex2(dt * Al[k]);
+          if (DISC == 0) st[k] = fmaf(ab, st[k] + Bu, -Bu);
+          else st[k] = fmaf(ab, st[k], A[k] * dt * Bu);
+        }
+      }
+      hist[(t + 1) * kBwdThreads + tid] = make_float4(st[0], st[1], st[2], st[3]);
+    }
+
+    // adjoint, backwards through the chunk
+    for (int t = tv - 1; t >= 0; --t) {
+      const int p = t * CB + c;
+      const float dt = f_dt[p], uu = f_u[p], dy = f_dy[p];
+      const float4 sn4 = hist[(t + 1) * kBwdThreads + tid], sp4 = hist[t * kBwdThreads + tid];
+      const float sn[4] = {sn4.x, sn4.y, sn4.z, sn4.w}, sp[4] = {sp4.x, sp4.y, sp4.z, sp4.w};
+      const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
+      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+      float dus = 0.0f, ddt = 0.0f, ys = 0.0f;
+      float v[8];  // dB partials (states n0..n0+3), then dC partials
+#pragma unroll
+      for (int k = 0; k < NPL; ++k) {
+        const float lam = fmaf(dy, Cv[k], carry[k]);
+        const float ht = PRECISE ? sn[k] : sn[k] * Ik[k];
+        const float Ahp = PRECISE ? A[k] * sp[k] : sp[k];  // A h_{t-1}
+        v[4 + k] = dy * ht;
+        ys = fmaf(Cv[k], ht, ys);
+        float ab, q;
+        if constexpr (PRECISE) {
+          const float e = expm1f(dt * A[k]);
+          ab = 1.0f + e;
+          q = DISC ? dt : e * Ik[k];
+        } else {
+          ab = hw_ex2(dt * Al[k]);
+          q = DISC ? dt : (ab - 1.0f) * Ik[k];
+        }
+        const float Bu = Bv[k] * uu;
+        const float al = ab * lam;
+        const float r = lam * q;
+        float m;
+        if (DISC == 0) {
+          m = al * (Ahp + Bu);
+          dAl[k] = fmaf(dt, m, dAl[k]);
+          dAl[k] = fmaf(-r, Bu, dAl[k]);
+        } else {
+          m = fmaf(al, Ahp, lam * Bu);
+          dAl[k] = fmaf(dt * al, Ahp, dAl[k]);
+        }
+        ddt += m;
+        v[k] = r * uu;
+        dus = fmaf(r, Bv[k], dus);
+        carry[k] = al;
+      }
+#pragma unroll
+      for (int o = 1; o < LPC; o <<= 1) {
+        dus += __shfl_xor_sync(0xffffffffu, dus, o);
+        ddt += __shfl_xor_sync(0xffffffffu, ddt, o);
+        ys += __shfl_xor_sync(0xffffffffu, ys, o);
+      }
+      // dB, dC summed over the channels of this warp (lane bits >= LPC)
+      int jh = 0;
+      if constexpr (LPC <= 16) { reduce_scatter<8>(v, lane, 16); jh = (lane >> 4) & 1; }
+      if constexpr (LPC <= 8) { reduce_scatter<4>(v, lane, 8); jh = jh * 2 + ((lane >> 3) & 1); }
+      if constexpr (LPC <= 4) { reduce_scatter<2>(v, lane, 4); jh = jh * 2 + ((lane >> 2) & 1); }
+      constexpr int W = (LPC <= 4) ? 1 : (LPC <= 8 ? 2 : (LPC <= 16 ? 4 : 8));
+#pragma unroll
+      for (int i = 0; i < W; ++i) {
+        const int j = jh * W + i;  // 0..3: dB of state n0 + j; 4..7: dC of state n0 + j - 4
+        atomicAdd(&acc[t * 2 * N + (j >> 2) * N + n0 + (j & 3)], v[i]);
+      }
+      if (part == 0 && cv) {
+        const float Dd = ch_D[c];
+        const float dd = ddt * f_sg[p];
+        E::store(os + p, fmaf(dy, Dd, dus));
+        E::store(os + K * CB + p, dd);
+        if (has_z) E::store(os + 2 * K * CB + p, fmaf(Dd, uu, ys) * f_dz[p]);
+        dD_acc = fmaf(dy, uu, dD_acc);
+        dbias_acc += dd;
+      }
+    }
+    __syncthreads();
+    for (int i = tid * 4; i < K * 2 * N; i += kBwdThreads * 4) {
+      const int t = i / (2 * N), j = i - t * 2 * N;
+      if (t < tv) {
+        float* dst = (j < N ? a.dB : a.dC) + (rowb + t0 + t) * N + (j < N ? j : j - N);
+        atomicAdd(reinterpret_cast<float4*>(dst), *reinterpret_cast<const float4*>(acc + i));
+      }
+      st4(acc + i, zero4);
+    }
+    OCopy3::smem_to_global(sm + G::oO, dst_o, rowb + t0, Dm, d0, nch, tv, tid);
+  }
+
+  if (cv) {
+    atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), make_float4(dAl[0], dAl[1], dAl[2], dAl[3]));
+    if (a.dh0) st4(a.dh0 + ((size_t)b * Dm + d) * N + n0, make_float4(carry[0], carry[1], carry[2], carry[3]));
+    if (part == 0) {
+      if (a.dD) atomicAdd(a.dD + d, dD_acc);
+      if (a.ddelta_bias) atomicAdd(a.ddelta_bias + d, dbias_acc);
+    }
+  }
+}
+
+template <typename Tin, int N, int DISC, bool ALIGNED>
+cudaError_t launch_bwd_variant(const BwdArgs& a, cudaStream_t stream) {
+  using G = BwdGeom<Tin, N, ALIGNED>;
+  static bool configured = false;  // per instantiation; benign race (idempotent)
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<Tin, N, DISC, ALIGNED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const dim3 grid((a.dim + G::CB - 1) / G::CB, a.batch);
+  scan_bwd_kernel<Tin, N, DISC, ALIGNED><<<grid, kBwdThreads, G::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename Tin, int N>
+cudaError_t launch_bwd_n(const BwdArgs& a, cudaStream_t stream) {
+  if (a.disc == 0)
+    return a.aligned ? launch_bwd_variant<Tin, N, 0, true>(a, stream) : launch_bwd_variant<Tin, N, 0, false>(a, stream);
+  return a.aligned ? launch_bwd_variant<Tin, N, 1, true>(a, stream) : launch_bwd_variant<Tin, N, 1, false>(a, stream);
+}
+
+template <typename Tin>
+cudaError_t launch_bwd_typed(const BwdArgs& a, cudaStream_t stream) {
+  switch (a.dstate) {
+    case 16: return launch_bwd_n<Tin, 16>(a, stream);
+    case 32: return launch_bwd_n<Tin, 32>(a, stream);
+    case 64: return launch_bwd_n<Tin, 64>(a, stream);
+    case 128: return launch_bwd_n<Tin, 128>(a, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool scan_bwd_supported(int dstate) { return dstate == 16 || dstate == 32 || dstate == 64 || dstate == 128; }
+
+cudaError_t launch_scan_bwd(int dtype, const BwdArgs& a, cudaStream_t stream) {
+  return dtype == 0 ? launch_bwd_typed<float>(a, stream) : launch_bwd_typed<__nv_bfloat16>(a, stream);
+}
+
+}  // namespace mamba

@@ -228,3 +228,15 @@ def make_decode_inputs(batch: int, dim: int, dstate: int, dtype: str, seed: int,
 def make_decode_config_inputs(cfg: DecodeConfig, seed: int) -> dict:
     return make_decode_inputs(cfg.batch, cfg.dim, cfg.dstate, cfg.dtype, seed,
                               cfg.pool, cfg.dt_range)
+
+
+def make_bwd_inputs(batch: int, dim: int, dstate: int, seqlen: int, dtype: str,
+                    seed: int, dt_range=(1e-3, 1e-1)) -> dict:
+    """Seeded inputs of the backward scan: the scan inputs of ``make_scan_inputs``
+    plus dout (batch, seqlen, dim) in ``dtype``, and h0, dlast (batch, dim, dstate)
+    fp32, all N(0, 1)."""
+    inp = make_scan_inputs(batch, dim, dstate, seqlen, dtype, seed, dt_range)
+    inp["dout"] = _draw_normal(seed, 7, (batch, seqlen, dim), dtype)
+    inp["h0"] = _draw_normal(seed, 8, (batch, dim, dstate), "f32")
+    inp["dlast"] = _draw_normal(seed, 9, (batch, dim, dstate), "f32")
+    return inp

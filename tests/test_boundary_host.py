@@ -127,3 +127,42 @@ def test_conv_scan_rejects_bad_arguments(lib):
     assert lib.mamba_conv1d_selective_scan_fwd(*args(4, w=None)) == 1  # no taps
     p = ScanPlan(0, 0, 0, 1)
     assert lib.mamba_conv1d_selective_scan_fwd(*args(4, plan=ctypes.byref(p))) == 2  # simplified + conv
+
+
+def _bwd_args(batch=2, dim=8, dstate=16, seqlen=4, dtype=1, disc=0, **over):
+    """Arguments of mamba_selective_scan_bwd with distinct fake 16-byte-aligned pointers."""
+    names = ["u", "delta", "A_log", "B", "C", "D", "z", "delta_bias", "initial_state", "dout", "dlast_state",
+             "du", "ddelta", "dA_log", "dB", "dC", "dD", "dz", "ddelta_bias", "dinitial_state"]
+    ptrs = {n: FAKE + (i + 1) * 0x1000000 for i, n in enumerate(names)}
+    for opt in ("D", "z", "delta_bias", "initial_state", "dlast_state", "dD", "dz", "ddelta_bias",
+                "dinitial_state"):
+        ptrs[opt] = None
+    ptrs.update(over)
+    return (batch, dim, dstate, seqlen, dtype, disc) + tuple(ptrs[n] for n in names) + (None,)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dstate=8), 2),                          # not built for this state size
+    (dict(dstate=256), 2),
+    (dict(disc=2), 1),                            # unknown discretisation
+    (dict(dtype=7), 1),
+    (dict(seqlen=-1), 1),
+    (dict(dstate=0), 1),
+    (dict(batch=70000), 2),
+    (dict(dz=FAKE + 0x30000000), 1),              # dz without z
+    (dict(du=None), 1),                           # required output missing
+    (dict(dout=None), 1),
+    (dict(dA_log=FAKE + 0xE000004), 2),          # fp32 gradient array not 16-byte aligned
+    (dict(initial_state=FAKE + 0x9000008), 2),
+    (dict(du=FAKE + 0x1000000), 1),               # du is u
+    (dict(dB=FAKE + 0xC000010), 1),               # dB overlaps du
+])
+def test_bwd_rejects_bad_arguments(lib, kw, status):
+    over = {k: v for k, v in kw.items() if k not in ("batch", "dim", "dstate", "seqlen", "dtype", "disc")}
+    sizes = {k: v for k, v in kw.items() if k in ("batch", "dim", "dstate", "seqlen", "dtype", "disc")}
+    assert lib.mamba_selective_scan_bwd(*_bwd_args(**sizes, **over)) == status
+
+
+def test_bwd_empty_problem_is_ok_without_a_device(lib):
+    # nothing to zero and nothing to launch
+    assert lib.mamba_selective_scan_bwd(*_bwd_args(batch=0, dim=0)) == 0

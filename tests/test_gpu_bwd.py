@@ -1,0 +1,182 @@
+"""GPU parity of the backward scan against the fp64 gradient oracle, through the C ABI.
+
+Every gradient the call returns is compared element by element with
+``oracle.selective_scan_bwd`` on the same seeded inputs (bf16 inputs are
+widened exactly). Tolerances as for the forward (max relative error with an
+rms floor, helpers.parity_err): 1e-4 for fp32 inputs, 2e-2 for bf16 inputs.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import TOL, parity_err, to_numpy, to_torch
+from selective_state_space_125_b300.workloads import make_bwd_inputs
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("du", "ddelta", "dz", "dA_log", "dB", "dC", "dD", "ddelta_bias", "dh0")
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_125_b300 import build
+    build.build()
+    return torch.device("cuda:0")
+
+
+def run_gpu_bwd(inp, dev, disc=0, with_z=True, with_D=True, with_bias=True, with_h0=False, with_dlast=False):
+    import torch
+    from selective_state_space_125_b300 import binding
+    dt = inp["dtype"]
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    g = binding.mamba_selective_scan_bwd(
+        to_torch(inp["u"], dt, dev), to_torch(inp["delta"], dt, dev), f32(inp["A_log"]),
+        to_torch(inp["B"], dt, dev), to_torch(inp["C"], dt, dev), to_torch(inp["dout"], dt, dev),
+        D=f32(inp["D"]) if with_D else None, z=to_torch(inp["z"], dt, dev) if with_z else None,
+        delta_bias=f32(inp["delta_bias"]) if with_bias else None,
+        initial_state=f32(inp["h0"]) if with_h0 else None,
+        dlast_state=f32(inp["dlast"]) if with_dlast else None,
+        discretization=disc, need_dD=True, need_ddelta_bias=True, need_dinitial_state=True)
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    out = {k: (None if v is None else to_numpy(v)) for k, v in g.items()}
+    out["dh0"] = out.pop("dinitial_state")
+    return out
+
+
+def run_oracle_bwd(inp, disc=0, with_z=True, with_D=True, with_bias=True, with_h0=False, with_dlast=False):
+    dim = inp["u"].shape[2]
+    dstate = inp["A_log"].shape[1]
+    batch = inp["u"].shape[0]
+    # an absent D / bias / h0 is 0: pass zeros so that the oracle returns their gradients too
+    g = oracle.selective_scan_bwd(
+        inp["u"], inp["delta"], inp["A_log"], inp["B"], inp["C"], inp["dout"],
+        D=inp["D"] if with_D else np.zeros(dim), z=inp["z"] if with_z else None,
+        delta_bias=inp["delta_bias"] if with_bias else np.zeros(dim),
+        h0=inp["h0"] if with_h0 else np.zeros((batch, dim, dstate)),
+        dlast=inp["dlast"] if with_dlast else None, variant=disc)
+    return g
+
+
+def assert_grads(got, ref, dtype, what):
+    errs = {}
+    for k in GRADS:
+        if ref.get(k) is None:
+            assert got.get(k) is None, f"{what}: {k} returned without its input"
+            continue
+        errs[k] = parity_err(got[k], ref[k])
+    bad = {k: e for k, e in errs.items() if not e <= TOL[dtype]}
+    assert not bad, f"{what}: " + ", ".join(f"{k} {e:.2e}" for k, e in sorted(errs.items()))
+    return errs
+
+
+def check(batch, dim, dstate, seqlen, dtype, seed=0, disc=0, **opts):
+    inp = make_bwd_inputs(batch, dim, dstate, seqlen, dtype, seed)
+    got = run_gpu_bwd(inp, dev_holder["dev"], disc, **opts)
+    ref = run_oracle_bwd(inp, disc, **opts)
+    return assert_grads(got, ref, dtype, f"B{batch} D{dim} N{dstate} L{seqlen} {dtype} disc{disc} {opts}")
+
+
+dev_holder = {}
+
+
+@pytest.fixture(autouse=True)
+def _dev(dev):
+    dev_holder["dev"] = dev
+
+
+# Several 16-step chunks with a ragged tail; several channel blocks with a
+# ragged last block; the element-by-element loader (dim * 2 % 16 != 0).
+SHAPES = [
+    (2, 64, 16, 50),
+    (1, 40, 16, 33),      # channel blocks of 32: a ragged block of 8
+    (2, 36, 16, 20),      # bf16 rows not a multiple of 16 bytes -> element loads
+    (1, 64, 16, 1),       # L = 1
+    (1, 32, 16, 16),      # exactly one chunk
+    (3, 96, 16, 130),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_bwd_shapes(dtype, shape):
+    check(*shape, dtype, with_h0=True, with_dlast=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [32, 64, 128])
+def test_bwd_state_sizes(dtype, dstate):
+    check(2, 48, dstate, 37, dtype, seed=1, with_h0=True, with_dlast=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(with_z=False), dict(with_D=False), dict(with_bias=False),
+                                  dict(with_h0=False, with_dlast=False), dict(with_h0=True, with_dlast=False),
+                                  dict(with_h0=False, with_dlast=True)])
+def test_bwd_optional_arguments(dtype, opts):
+    check(2, 64, 16, 45, dtype, seed=2, **opts)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dstate", [16, 64])
+def test_bwd_simplified_discretisation(dtype, dstate):
+    check(2, 64, dstate, 41, dtype, seed=3, disc=1, with_h0=True, with_dlast=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_long_sequence(dtype):
+    # many chunks: the checkpoint chain and the adjoint carry over 64 chunks
+    check(1, 64, 16, 1024, dtype, seed=4, with_h0=True, with_dlast=True)
+
+
+def test_bwd_wide_dt_range():
+    # dt over [1e-4, 1] (the long-sequence range): tiny and large dt A
+    inp = make_bwd_inputs(2, 64, 16, 70, "f32", 5, dt_range=(1e-4, 1.0))
+    dev = dev_holder["dev"]
+    got = run_gpu_bwd(inp, dev, with_h0=True, with_dlast=True)
+    ref = run_oracle_bwd(inp, with_h0=True, with_dlast=True)
+    assert_grads(got, ref, "f32", "dt in [1e-4, 1]")
+
+
+def test_bwd_empty_sequence():
+    import torch
+    from selective_state_space_125_b300 import binding
+    dev = dev_holder["dev"]
+    inp = make_bwd_inputs(2, 32, 16, 0, "f32", 6)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    g = binding.mamba_selective_scan_bwd(
+        f32(inp["u"]), f32(inp["delta"]), f32(inp["A_log"]), f32(inp["B"]), f32(inp["C"]), f32(inp["dout"]),
+        D=f32(inp["D"]), delta_bias=f32(inp["delta_bias"]), initial_state=f32(inp["h0"]),
+        dlast_state=f32(inp["dlast"]))
+    torch.cuda.synchronize()
+    assert np.array_equal(to_numpy(g["dinitial_state"]), inp["dlast"])   # last_state = initial_state
+    assert not to_numpy(g["dA_log"]).any() and not to_numpy(g["dD"]).any()
+    assert not to_numpy(g["ddelta_bias"]).any()
+
+
+def test_bwd_unsupported_state_size_raises():
+    import torch
+    from selective_state_space_125_b300 import binding
+    dev = dev_holder["dev"]
+    inp = make_bwd_inputs(1, 16, 8, 4, "f32", 7)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    with pytest.raises(binding.MambaError) as ei:
+        binding.mamba_selective_scan_bwd(f32(inp["u"]), f32(inp["delta"]), f32(inp["A_log"]), f32(inp["B"]),
+                                         f32(inp["C"]), f32(inp["dout"]))
+    assert ei.value.status == 2
+
+
+def test_bwd_repeatable_up_to_atomics():
+    # two calls on the same inputs: per-element outputs are identical; the
+    # atomic sums (dB, dC, dA_log, dD, ddelta_bias) agree to rounding
+    inp = make_bwd_inputs(2, 64, 16, 40, "f32", 8)
+    dev = dev_holder["dev"]
+    g1 = run_gpu_bwd(inp, dev)
+    g2 = run_gpu_bwd(inp, dev)
+    for k in ("du", "ddelta", "dz"):
+        assert np.array_equal(g1[k], g2[k]), k
+    for k in ("dB", "dC", "dA_log", "dD", "ddelta_bias"):
+        assert parity_err(g1[k], g2[k]) < 1e-5, k
