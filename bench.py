@@ -38,6 +38,12 @@ FP32_LANES_PER_SM = 128          # FP32 lanes per SM (B300): one FMUL/FADD/FFMA 
 # the input product, the two FMAs of the state update and the two of the
 # readout (C / A times the scaled state, accumulated); exp runs on MUFU.
 ALG_OPS_PER_STATE_STEP = 6
+# FP32 lane-ops per (channel, step, state) that the backward needs given the
+# forward states: one forward update to recompute h (4: dt*A, B*u, the add and
+# the FMA of the scaled update) and the adjoint step (16: lambda, h_t and its
+# dC product, dt*A, (abar-1)/A (2), B*u, A h_{t-1} + B u, abar*lambda, the dt
+# term and its sum, the two dA_log FMAs, lambda*q, its dB and du products).
+ALG_BWD_OPS_PER_STATE_STEP = 20
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_traffic.json")
 
 
@@ -56,6 +62,7 @@ def parse():
     p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
     p.add_argument("--no-decode", action="store_true", help="skip the full-size decode measurement")
     p.add_argument("--no-variants", action="store_true", help="skip the simplified-discretisation scan timing")
+    p.add_argument("--no-bwd", action="store_true", help="skip the backward-scan timing")
     p.add_argument("--decode-only", action="store_true",
                    help="time only the decode step on the full decode workloads and print their JSON")
     p.add_argument("--decode-workload", default="both", choices=["both", "decode", "decode128"])
@@ -417,6 +424,37 @@ def run_ours(args, rank, world, device):
                   "achieved": sops / (sms_ / 1e3) / 1e12, "unit": "T FP32 lane-op/s",
                   "frac": sops / (sms_ / 1e3) / 1e12 / peak_tops, "ops_per_launch": sops,
                   "hbm_frac": alg_bytes / (sms_ / 1e3) / 1e9 / peaks["hbm_gbs"], "calls": nv}
+    # The backward scan on the same inputs: gradients of every input for a random dout.
+    bwd = None
+    if not args.no_bwd:
+        gen = torch.Generator(device).manual_seed(11)
+        douts = [torch.randn((B, L, Dm), device=device, generator=gen).to(tdt) for _ in range(nsets)]
+
+        def bwd_call(i):
+            s = sets[i % nsets]
+            return binding.mamba_selective_scan_bwd(s["u"], s["delta"], A_log, s["B"], s["C"], douts[i % nsets],
+                                                    D=Dv, z=s["z"], delta_bias=bias)
+        for i in range(3):
+            bwd_call(i)
+        torch.cuda.synchronize(device)
+        nb = 20
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for i in range(nb):
+            bwd_call(i)
+        b1.record(stream)
+        torch.cuda.synchronize(device)
+        bms = b0.elapsed_time(b1) / nb
+        bops = ALG_BWD_OPS_PER_STATE_STEP * N * B * L * Dm
+        bbytes = (7 * es * B * L * Dm + 2 * N * es * B * L + 2 * N * 4 * B * L + 2 * Dm * N * 4 + 4 * Dm * 4)
+        bwd = {"step": "backward scan: du, ddelta, dz, dA_log, dB, dC, dD, ddelta_bias for a random dout "
+                       "(5 memsets + 1 kernel launch per call)",
+               "ms_per_call": bms, "channel_steps_per_s": B * L * Dm / (bms / 1e3),
+               "achieved": bops / (bms / 1e3) / 1e12, "unit": "T FP32 lane-op/s",
+               "frac": bops / (bms / 1e3) / 1e12 / peak_tops, "ops_per_call": bops,
+               "hbm_bytes_per_call": bbytes, "hbm_frac": bbytes / (bms / 1e3) / 1e9 / peaks["hbm_gbs"],
+               "calls": nb}
+        del douts
     result = {
         "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -447,6 +485,8 @@ def run_ours(args, rank, world, device):
     if simple is not None:
         result["scan_simplified"] = simple
         result["scan_conv1d_fused"] = conv
+    if bwd is not None:
+        result["scan_bwd"] = bwd
     return result
 
 

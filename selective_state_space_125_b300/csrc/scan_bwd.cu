@@ -65,14 +65,17 @@ struct BwdGeom {
   static constexpr size_t oX = 0;                                      // raw u, delta, z, dout tiles
   static constexpr size_t oBC = align16(oX + 4 * szX);                 // raw B, C tiles
   static constexpr size_t oO = align16(oBC + 2 * szBC);                // raw du, ddelta, dz tiles
-  static constexpr size_t oF = align16(oO + 3 * szX);                  // dt, sigmoid, dy, dz factor, u
-  static constexpr size_t oBf = oF + 5 * szF;                          // B, C as float
+  static constexpr size_t oTC = align16(oO + 3 * szX);                 // [K][CB] float4 (dt, u, dy, sigmoid)
+  static constexpr size_t oDz = oTC + 4 * szF;                         // [K][CB] dz factor
+  static constexpr size_t oRed = oDz + szF;                            // [3][K][CB] sums over states
+  static constexpr size_t oBf = oRed + 3 * szF;                        // B, C as float
   static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [K][2N] dB | dC of the chunk
   static constexpr size_t oCh = oAcc + size_t(K) * 2 * N * 4;          // per-channel bias, D
   static constexpr size_t oHist = align16(oCh + 2 * size_t(CB) * 4);   // [K+1][threads] states
   static constexpr size_t kSmem = oHist + size_t(K + 1) * kBwdThreads * 16;
   static_assert(N % 16 == 0 && LPC <= 32, "state size must be 16, 32, 64 or 128");
   static_assert((CB * ES) % SBX == 0 && (N * ES) % SBB == 0, "slot width must divide a tile row");
+  static_assert(kBwdThreads % CB == 0, "a thread's epilogue channel is tid % CB");
 };
 
 // Copies of NT tiles of [K][W] elements between global memory and shared
@@ -141,6 +144,128 @@ __device__ __forceinline__ void reduce_scatter(float* v, int lane, int m) {
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(hw_ex2(x.x), hw_ex2(x.y)); }
+
+// ---------------------------------------------------- forward step (4 states)
+// bf16 inputs: scaled state s = A h in two packed pairs; Al = A log2(e).
+template <int DISC>
+__device__ __forceinline__ void fwd_step_fast(float2 (&s)[2], float4 B4, float dt, float uu, const float2 (&Al)[2],
+                                              const float2 (&A)[2]) {
+  const float2 dd = dup2(dt), u2 = dup2(uu), nu = dup2(-uu);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
+    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    if (DISC == 0) {
+      s[h] = __ffma2_rn(ab, __ffma2_rn(Bp, u2, s[h]), __fmul2_rn(Bp, nu));  // abar (s + B u) - B u
+    } else {
+      s[h] = __ffma2_rn(ab, s[h], __fmul2_rn(__fmul2_rn(A[h], dd), __fmul2_rn(Bp, u2)));  // abar s + A dt B u
+    }
+  }
+}
+
+// fp32 inputs: h itself, expm1f.
+template <int DISC>
+__device__ __forceinline__ void fwd_step_precise(float (&h)[4], float4 B4, float dt, float uu, const float (&A)[4],
+                                                 const float (&Ik)[4]) {
+  const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float e = expm1f(dt * A[k]);
+    const float q = DISC ? dt : e * Ik[k];
+    h[k] = fmaf(e, h[k], fmaf(q, Bv[k] * uu, h[k]));  // (1 + e) h + q B u
+  }
+}
+
+// ---------------------------------------------------- adjoint step (4 states)
+// Given s_t (sn), s_{t-1} (sp) and lambda_{t+1} abar_{t+1} (carry): updates
+// carry to abar_t lambda_t, adds the dA_log terms, writes the dB partials to
+// v[0..3] and the dC partials to v[4..7], and returns the sums over the 4
+// states of the du, dt and y terms.
+template <int DISC>
+__device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, float4 C4, float dt, float uu, float dy,
+                                              float2 (&carry)[2], float2 (&dApos)[2], float2 (&dAneg)[2],
+                                              const float2 (&Al)[2], const float2 (&Ik)[2], float (&v)[8],
+                                              float& dus, float& ddt, float& ys) {
+  const float2 dd = dup2(dt), u2 = dup2(uu), yy = dup2(dy);
+  float2 sdus = make_float2(0.f, 0.f), sddt = sdus, sys = sdus;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
+    const float2 Cp = h == 0 ? lo2(C4) : hi2(C4);
+    const float2 snp = h == 0 ? lo2(sn) : hi2(sn);
+    const float2 spp = h == 0 ? lo2(sp) : hi2(sp);  // A h_{t-1}
+    const float2 lam = __ffma2_rn(yy, Cp, carry[h]);
+    const float2 ht = __fmul2_rn(snp, Ik[h]);
+    const float2 dc = __fmul2_rn(yy, ht);
+    sys = __ffma2_rn(Cp, ht, sys);
+    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    const float2 Bu = __fmul2_rn(Bp, u2);
+    const float2 al = __fmul2_rn(ab, lam);
+    float2 r, m;
+    if (DISC == 0) {
+      const float2 q = __fmul2_rn(__fadd2_rn(ab, make_float2(-1.f, -1.f)), Ik[h]);  // (abar - 1) / A
+      r = __fmul2_rn(lam, q);
+      m = __fmul2_rn(al, __fadd2_rn(spp, Bu));                  // abar lambda (A h_{t-1} + B u)
+      dApos[h] = __ffma2_rn(dd, m, dApos[h]);                   // + dt abar lambda v
+      dAneg[h] = __ffma2_rn(r, Bu, dAneg[h]);                   // - q lambda B u
+    } else {
+      r = __fmul2_rn(lam, dd);
+      m = __ffma2_rn(al, spp, __fmul2_rn(lam, Bu));             // lambda (abar A h_{t-1} + B u)
+      dApos[h] = __ffma2_rn(__fmul2_rn(dd, al), spp, dApos[h]); // + dt abar lambda A h_{t-1}
+    }
+    const float2 db = __fmul2_rn(r, u2);
+    sdus = __ffma2_rn(r, Bp, sdus);
+    sddt = __fadd2_rn(sddt, m);
+    carry[h] = al;
+    v[2 * h] = db.x;
+    v[2 * h + 1] = db.y;
+    v[4 + 2 * h] = dc.x;
+    v[4 + 2 * h + 1] = dc.y;
+  }
+  dus = sdus.x + sdus.y;
+  ddt = sddt.x + sddt.y;
+  ys = sys.x + sys.y;
+}
+
+template <int DISC>
+__device__ __forceinline__ void adj_step_precise(float4 sn4, float4 sp4, float4 B4, float4 C4, float dt, float uu,
+                                                 float dy, float (&carry)[4], float (&dAl)[4], const float (&A)[4],
+                                                 const float (&Ik)[4], float (&v)[8], float& dus, float& ddt,
+                                                 float& ys) {
+  const float sn[4] = {sn4.x, sn4.y, sn4.z, sn4.w}, sp[4] = {sp4.x, sp4.y, sp4.z, sp4.w};
+  const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+  dus = ddt = ys = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lam = fmaf(dy, Cv[k], carry[k]);
+    const float Ahp = A[k] * sp[k];
+    v[4 + k] = dy * sn[k];
+    ys = fmaf(Cv[k], sn[k], ys);
+    const float e = expm1f(dt * A[k]);
+    const float ab = 1.0f + e;
+    const float Bu = Bv[k] * uu;
+    const float al = ab * lam;
+    float r, m;
+    if (DISC == 0) {
+      r = lam * (e * Ik[k]);
+      m = al * (Ahp + Bu);
+      dAl[k] = fmaf(dt, m, dAl[k]);
+      dAl[k] = fmaf(-r, Bu, dAl[k]);
+    } else {
+      r = lam * dt;
+      m = fmaf(al, Ahp, lam * Bu);
+      dAl[k] = fmaf(dt * al, Ahp, dAl[k]);
+    }
+    ddt += m;
+    v[k] = r * uu;
+    dus = fmaf(r, Bv[k], dus);
+    carry[k] = al;
+  }
+}
 
 template <typename Tin, int N, int DISC, bool ALIGNED>
 __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) {
@@ -158,11 +283,9 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
   const Tin* xs = reinterpret_cast<const Tin*>(sm + G::oX);
   const Tin* bs = reinterpret_cast<const Tin*>(sm + G::oBC);
   Tin* os = reinterpret_cast<Tin*>(sm + G::oO);
-  float* f_dt = reinterpret_cast<float*>(sm + G::oF);
-  float* f_sg = f_dt + K * CB;
-  float* f_dy = f_sg + K * CB;
-  float* f_dz = f_dy + K * CB;
-  float* f_u = f_dz + K * CB;
+  float4* f_tc = reinterpret_cast<float4*>(sm + G::oTC);
+  float* f_dz = reinterpret_cast<float*>(sm + G::oDz);
+  float* red = reinterpret_cast<float*>(sm + G::oRed);
   float* f_B = reinterpret_cast<float*>(sm + G::oBf);
   float* f_C = f_B + K * N;
   float* acc = reinterpret_cast<float*>(sm + G::oAcc);
@@ -193,31 +316,52 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
   for (int i = tid; i < K * 2 * N; i += kBwdThreads) acc[i] = 0.0f;
 
   // A = -exp(A_log), 1/A and (fast path) A log2(e) for my states.
-  float A[NPL], Al[NPL], Ik[NPL];
+  float A[NPL], Ik[NPL];
+  float2 A2[2], Al2[2], Ik2[2];
 #pragma unroll
   for (int k = 0; k < NPL; ++k) {
     const float al = cv ? a.A_log[(size_t)d * N + n0 + k] : 0.0f;
     if constexpr (PRECISE) {
       A[k] = -expf(al);
       Ik[k] = 1.0f / A[k];
-      Al[k] = A[k];
     } else {
       A[k] = -hw_ex2(al * kLog2e);
       Ik[k] = hw_rcp(A[k]);
-      Al[k] = A[k] * kLog2e;
     }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    A2[h] = make_float2(A[2 * h], A[2 * h + 1]);
+    Al2[h] = make_float2(A[2 * h] * kLog2e, A[2 * h + 1] * kLog2e);
+    Ik2[h] = make_float2(Ik[2 * h], Ik[2 * h + 1]);
   }
 
-  // ------------------------------------------------ phase 1: checkpoints
-  float s[NPL];  // h (fp32 inputs) or A h (bf16 inputs)
-  {
-    const float4 h = (cv && a.h0) ? ld4(a.h0 + ((size_t)b * Dm + d) * N + n0) : zero4;
-    s[0] = h.x; s[1] = h.y; s[2] = h.z; s[3] = h.w;
-    if constexpr (!PRECISE) {
-#pragma unroll
-      for (int k = 0; k < NPL; ++k) s[k] *= A[k];
+  // state: h (fp32 inputs) or s = A h as two pairs (bf16 inputs)
+  float hs[NPL];
+  float2 s2[2];
+  auto load_state = [&](float4 h) {
+    if constexpr (PRECISE) {
+      hs[0] = h.x; hs[1] = h.y; hs[2] = h.z; hs[3] = h.w;
+    } else {
+      s2[0] = __fmul2_rn(lo2(h), A2[0]);
+      s2[1] = __fmul2_rn(hi2(h), A2[1]);
     }
-  }
+  };
+  auto state4 = [&]() -> float4 {  // the state as stored in the history (h or s)
+    if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
+    else return make_float4(s2[0].x, s2[0].y, s2[1].x, s2[1].y);
+  };
+  auto state_h4 = [&]() -> float4 {  // h itself
+    if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
+    else return make_float4(s2[0].x * Ik[0], s2[0].y * Ik[1], s2[1].x * Ik[2], s2[1].y * Ik[3]);
+  };
+  auto fwd_step = [&](float4 B4, float dt, float uu) {
+    if constexpr (PRECISE) fwd_step_precise<DISC>(hs, B4, dt, uu, A, Ik);
+    else fwd_step_fast<DISC>(s2, B4, dt, uu, Al2, A2);
+  };
+
+  // ------------------------------------------------ phase 1: checkpoints
+  load_state((cv && a.h0) ? ld4(a.h0 + ((size_t)b * Dm + d) * N + n0) : zero4);
   {
     XCopy2 xp;
     BCopy1 bp;
@@ -228,12 +372,7 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
       bp.load(src_b, rowb, N, 0, N, K, tid);
     }
     for (int ci = 0; ci < nck; ++ci) {
-      if (cv) {
-        float4 h;
-        if constexpr (PRECISE) h = make_float4(s[0], s[1], s[2], s[3]);
-        else h = make_float4(s[0] * Ik[0], s[1] * Ik[1], s[2] * Ik[2], s[3] * Ik[3]);
-        st4(ckp + ci * ck_stride, h);
-      }
+      if (cv) st4(ckp + ci * ck_stride, state_h4());
       if (ci == nck - 1) break;  // the last chunk's end state is not needed
       __syncthreads();
       xp.to_smem(sm + G::oX, tid);
@@ -245,41 +384,29 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
       }
       for (int p = tid; p < K * CB; p += kBwdThreads) {
         const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
-        f_dt[p] = PRECISE ? softplus_precise(x) : softplus_fast(x);
-        f_u[p] = E::load(xs + p);
+        f_tc[p] = make_float4(PRECISE ? softplus_precise(x) : softplus_fast(x), E::load(xs + p), 0.f, 0.f);
       }
       for (int p = tid; p < K * N; p += kBwdThreads) f_B[p] = E::load(bs + p);
       __syncthreads();
 #pragma unroll 4
       for (int t = 0; t < K; ++t) {
-        const float dt = f_dt[t * CB + c], uu = f_u[t * CB + c];
-        const float4 B4 = ld4(f_B + t * N + n0);
-        const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
-#pragma unroll
-        for (int k = 0; k < NPL; ++k) {
-          const float Bu = Bv[k] * uu;
-          if constexpr (PRECISE) {
-            const float e = expm1f(dt * A[k]);
-            const float q = DISC ? dt : e * Ik[k];
-            s[k] = fmaf(e, s[k], fmaf(q, Bu, s[k]));  // h <- (1 + e) h + q B u
-          } else {
-            const float ab = hw_ex2(dt * Al[k]);
-            if (DISC == 0) s[k] = fmaf(ab, s[k] + Bu, -Bu);  // s <- abar (s + B u) - B u
-            else s[k] = fmaf(ab, s[k], A[k] * dt * Bu);      // s <- abar s + A dt B u
-          }
-        }
+        const float4 tc = f_tc[t * CB + c];
+        fwd_step(ld4(f_B + t * N + n0), tc.x, tc.y);
       }
     }
   }
 
   // --------------------------------------------------- phase 2: adjoint
-  float carry[NPL];  // abar_{t+1} lambda_{t+1} (dlast before the last step)
+  float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs
+  float2 carry2[2], dApos[2], dAneg[2];               // bf16 inputs
   {
     const float4 g = (cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
     carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
+    carry2[0] = lo2(g);
+    carry2[1] = hi2(g);
+    dApos[0] = dApos[1] = dAneg[0] = dAneg[1] = make_float2(0.f, 0.f);
   }
-  float dAl[NPL] = {0.f, 0.f, 0.f, 0.f};
-  float dD_acc = 0.0f, dbias_acc = 0.0f;
+  float dD_acc = 0.0f, dbias_acc = 0.0f;  // channel d0 + tid % CB
   XCopy4 xq;
   BCopy2 bq;
   auto src_x4 = [&](int tile) -> const void* {
@@ -309,18 +436,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
     for (int p = tid; p < K * CB; p += kBwdThreads) {
       const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
       const float g = E::load(xs + 3 * K * CB + p);
-      f_u[p] = E::load(xs + p);
-      f_dt[p] = PRECISE ? softplus_precise(x) : softplus_fast(x);
-      f_sg[p] = PRECISE ? sigmoid_precise(x) : sigmoid_fast(x);
+      const float dt = PRECISE ? softplus_precise(x) : softplus_fast(x);
+      const float sg = PRECISE ? sigmoid_precise(x) : sigmoid_fast(x);
+      float dy = g;
       if (has_z) {
         const float zz = E::load(xs + 2 * K * CB + p);
         const float sz = PRECISE ? sigmoid_precise(zz) : sigmoid_fast(zz);
-        f_dy[p] = g * zz * sz;                           // dloss/dy = dout SiLU(z)
+        dy = g * zz * sz;                              // dloss/dy = dout SiLU(z)
         f_dz[p] = g * sz * fmaf(zz, 1.0f - sz, 1.0f);  // dloss/dz = y * this
-      } else {
-        f_dy[p] = g;
-        f_dz[p] = 0.0f;
       }
+      f_tc[p] = make_float4(dt, E::load(xs + p), dy, sg);
     }
     for (int p = tid; p < K * N; p += kBwdThreads) {
       f_B[p] = E::load(bs + p);
@@ -329,81 +454,33 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
     __syncthreads();
 
     // recompute the chunk's states: hist[t + 1] = state after step t0 + t
-    float st[NPL] = {cks.x, cks.y, cks.z, cks.w};
-    if constexpr (!PRECISE) {
-#pragma unroll
-      for (int k = 0; k < NPL; ++k) st[k] *= A[k];
-    }
-    hist[tid] = make_float4(st[0], st[1], st[2], st[3]);
+    load_state(cks);
+    hist[tid] = state4();
 #pragma unroll 4
     for (int t = 0; t < tv; ++t) {
-      const float dt = f_dt[t * CB + c], uu = f_u[t * CB + c];
-      const float4 B4 = ld4(f_B + t * N + n0);
-      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
-#pragma unroll
-      for (int k = 0; k < NPL; ++k) {
-        const float Bu = Bv[k] * uu;
-        if constexpr (PRECISE) {
-          const float e = expm1f(dt * A[k]);
-          const float q = DISC ? dt : e * Ik[k];
-          st[k] = fmaf(e, st[k], fmaf(q, Bu, st[k]));
-        } else {
-          const float ab = hw_ex2(dt * Al[k]);
-          if (DISC == 0) st[k] = fmaf(ab, st[k] + Bu, -Bu);
-          else st[k] = fmaf(ab, st[k], A[k] * dt * Bu);
-        }
-      }
-      hist[(t + 1) * kBwdThreads + tid] = make_float4(st[0], st[1], st[2], st[3]);
+      const float4 tc = f_tc[t * CB + c];
+      fwd_step(ld4(f_B + t * N + n0), tc.x, tc.y);
+      hist[(t + 1) * kBwdThreads + tid] = state4();
     }
 
     // adjoint, backwards through the chunk
+    float4 sn = state4();  // state after the chunk's last valid step
     for (int t = tv - 1; t >= 0; --t) {
-      const int p = t * CB + c;
-      const float dt = f_dt[p], uu = f_u[p], dy = f_dy[p];
-      const float4 sn4 = hist[(t + 1) * kBwdThreads + tid], sp4 = hist[t * kBwdThreads + tid];
-      const float sn[4] = {sn4.x, sn4.y, sn4.z, sn4.w}, sp[4] = {sp4.x, sp4.y, sp4.z, sp4.w};
+      const float4 tc = f_tc[t * CB + c];
+      const float4 sp = hist[t * kBwdThreads + tid];
       const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
-      const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
-      float dus = 0.0f, ddt = 0.0f, ys = 0.0f;
-      float v[8];  // dB partials (states n0..n0+3), then dC partials
+      float v[8], dus, ddt, ys;
+      if constexpr (PRECISE) adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
+      else adj_step_fast<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, Al2, Ik2, v, dus, ddt, ys);
+      sn = sp;
+      // (du, dt, y) sums over the channel's LPC lanes: lane part & 3 keeps one of them
+      {
+        float w[4] = {dus, ddt, ys, 0.0f};
+        reduce_scatter<4>(w, lane, 2);
+        reduce_scatter<2>(w, lane, 1);
 #pragma unroll
-      for (int k = 0; k < NPL; ++k) {
-        const float lam = fmaf(dy, Cv[k], carry[k]);
-        const float ht = PRECISE ? sn[k] : sn[k] * Ik[k];
-        const float Ahp = PRECISE ? A[k] * sp[k] : sp[k];  // A h_{t-1}
-        v[4 + k] = dy * ht;
-        ys = fmaf(Cv[k], ht, ys);
-        float ab, q;
-        if constexpr (PRECISE) {
-          const float e = expm1f(dt * A[k]);
-          ab = 1.0f + e;
-          q = DISC ? dt : e * Ik[k];
-        } else {
-          ab = hw_ex2(dt * Al[k]);
-          q = DISC ? dt : (ab - 1.0f) * Ik[k];
-        }
-        const float Bu = Bv[k] * uu;
-        const float al = ab * lam;
-        const float r = lam * q;
-        float m;
-        if (DISC == 0) {
-          m = al * (Ahp + Bu);
-          dAl[k] = fmaf(dt, m, dAl[k]);
-          dAl[k] = fmaf(-r, Bu, dAl[k]);
-        } else {
-          m = fmaf(al, Ahp, lam * Bu);
-          dAl[k] = fmaf(dt * al, Ahp, dAl[k]);
-        }
-        ddt += m;
-        v[k] = r * uu;
-        dus = fmaf(r, Bv[k], dus);
-        carry[k] = al;
-      }
-#pragma unroll
-      for (int o = 1; o < LPC; o <<= 1) {
-        dus += __shfl_xor_sync(0xffffffffu, dus, o);
-        ddt += __shfl_xor_sync(0xffffffffu, ddt, o);
-        ys += __shfl_xor_sync(0xffffffffu, ys, o);
+        for (int o = 4; o < LPC; o <<= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], o);
+        if (part < 3) red[part * K * CB + t * CB + c] = w[0];
       }
       // dB, dC summed over the channels of this warp (lane bits >= LPC)
       int jh = 0;
@@ -416,17 +493,20 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
         const int j = jh * W + i;  // 0..3: dB of state n0 + j; 4..7: dC of state n0 + j - 4
         atomicAdd(&acc[t * 2 * N + (j >> 2) * N + n0 + (j & 3)], v[i]);
       }
-      if (part == 0 && cv) {
-        const float Dd = ch_D[c];
-        const float dd = ddt * f_sg[p];
-        E::store(os + p, fmaf(dy, Dd, dus));
-        E::store(os + K * CB + p, dd);
-        if (has_z) E::store(os + 2 * K * CB + p, fmaf(Dd, uu, ys) * f_dz[p]);
-        dD_acc = fmaf(dy, uu, dD_acc);
-        dbias_acc += dd;
-      }
     }
     __syncthreads();
+    // per (t, channel): du = sum + dy D, ddelta = dt-sum * sigmoid, dz = (y-sum + D u) * factor
+    for (int p = tid; p < tv * CB; p += kBwdThreads) {
+      const int cc = p % CB;  // == tid % CB
+      const float4 tc = f_tc[p];
+      const float Dd = ch_D[cc];
+      const float dd = red[K * CB + p] * tc.w;
+      E::store(os + p, fmaf(tc.z, Dd, red[p]));
+      E::store(os + K * CB + p, dd);
+      if (has_z) E::store(os + 2 * K * CB + p, fmaf(Dd, tc.y, red[2 * K * CB + p]) * f_dz[p]);
+      dD_acc = fmaf(tc.z, tc.y, dD_acc);
+      dbias_acc += dd;
+    }
     for (int i = tid * 4; i < K * 2 * N; i += kBwdThreads * 4) {
       const int t = i / (2 * N), j = i - t * 2 * N;
       if (t < tv) {
@@ -435,16 +515,26 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
       }
       st4(acc + i, zero4);
     }
+    __syncthreads();
     OCopy3::smem_to_global(sm + G::oO, dst_o, rowb + t0, Dm, d0, nch, tv, tid);
   }
 
   if (cv) {
-    atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), make_float4(dAl[0], dAl[1], dAl[2], dAl[3]));
-    if (a.dh0) st4(a.dh0 + ((size_t)b * Dm + d) * N + n0, make_float4(carry[0], carry[1], carry[2], carry[3]));
-    if (part == 0) {
-      if (a.dD) atomicAdd(a.dD + d, dD_acc);
-      if (a.ddelta_bias) atomicAdd(a.ddelta_bias + d, dbias_acc);
+    float4 dA4, g4;
+    if constexpr (PRECISE) {
+      dA4 = make_float4(dAl[0], dAl[1], dAl[2], dAl[3]);
+      g4 = make_float4(carry[0], carry[1], carry[2], carry[3]);
+    } else {
+      dA4 = make_float4(dApos[0].x - dAneg[0].x, dApos[0].y - dAneg[0].y, dApos[1].x - dAneg[1].x,
+                        dApos[1].y - dAneg[1].y);
+      g4 = make_float4(carry2[0].x, carry2[0].y, carry2[1].x, carry2[1].y);
     }
+    atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), dA4);
+    if (a.dh0) st4(a.dh0 + ((size_t)b * Dm + d) * N + n0, g4);
+  }
+  if ((tid % CB) < nch) {
+    if (a.dD) atomicAdd(a.dD + d0 + tid % CB, dD_acc);
+    if (a.ddelta_bias) atomicAdd(a.ddelta_bias + d0 + tid % CB, dbias_acc);
   }
 }
 
