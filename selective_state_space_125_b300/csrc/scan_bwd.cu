@@ -24,9 +24,10 @@
 // (dA_log = A dA because A = -exp(A_log).) The sums over states of the dt and
 // u terms are reduced across the LPC threads of a channel with shuffles; the
 // sums of dB and dC over channels are reduce-scattered across the channels of
-// a warp, added across warps in shared memory and once per chunk into global
-// memory. Per-channel sums over the batch (dA_log, dD, ddelta_bias) are added
-// with one atomic per thread at the end.
+// a warp, summed across warps in shared memory and once per chunk into global
+// memory. The reduce-scatters run over several steps at once, so that their
+// shuffle latency is paid once per group of steps. Per-channel sums over the
+// batch (dA_log, dD, ddelta_bias) are added with one atomic per thread at the end.
 //
 // Math: bf16 inputs use MUFU ex2/rcp and keep the scaled state s = A h during
 // the recomputation (s_t = abar (s_{t-1} + B u) - B u, so A h_{t-1} is read
@@ -69,13 +70,20 @@ struct BwdGeom {
   static constexpr size_t oDz = oTC + 4 * szF;                         // [K][CB] dz factor
   static constexpr size_t oRed = oDz + szF;                            // [3][K][CB] sums over states
   static constexpr size_t oBf = oRed + 3 * szF;                        // B, C as float
-  static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [K][2N] dB | dC of the chunk
-  static constexpr size_t oCh = oAcc + size_t(K) * 2 * N * 4;          // per-channel bias, D
+  static constexpr int NW = kBwdThreads / 32;
+  static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [warps][K][2N] dB | dC of the chunk
+  static constexpr size_t oCh = oAcc + size_t(NW) * K * 2 * N * 4;     // per-channel bias, D
   static constexpr size_t oHist = align16(oCh + 2 * size_t(CB) * 4);   // [K+1][threads] states
   static constexpr size_t kSmem = oHist + size_t(K + 1) * kBwdThreads * 16;
   static_assert(N % 16 == 0 && LPC <= 32, "state size must be 16, 32, 64 or 128");
   static_assert((CB * ES) % SBX == 0 && (N * ES) % SBB == 0, "slot width must divide a tile row");
   static_assert(kBwdThreads % CB == 0, "a thread's epilogue channel is tid % CB");
+  // Reduce-scatters run over SBT steps at once: R = log2(channels per warp)
+  // rounds for dB/dC leave VPL values per lane (4, or 8 when a warp holds one
+  // channel); the (du, dt, y) sums take 2 rounds plus log2(LPC / 4) butterflies.
+  static constexpr int R = (LPC == 4) ? 3 : (LPC == 8 ? 2 : (LPC == 16 ? 1 : 0));
+  static constexpr int SBT = (R >= 2) ? (1 << R) / 2 : 1;
+  static constexpr int VPL = (8 * SBT) >> R;
 };
 
 // Copies of NT tiles of [K][W] elements between global memory and shared
@@ -268,7 +276,7 @@ __device__ __forceinline__ void adj_step_precise(float4 sn4, float4 sp4, float4 
 }
 
 template <typename Tin, int N, int DISC, bool ALIGNED>
-__global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs a) {
   using G = BwdGeom<Tin, N, ALIGNED>;
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
@@ -313,7 +321,6 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
     ch_bias[tid] = (ok && a.delta_bias) ? a.delta_bias[d0 + tid] : 0.0f;
     ch_D[tid] = (ok && a.D) ? a.D[d0 + tid] : 0.0f;
   }
-  for (int i = tid; i < K * 2 * N; i += kBwdThreads) acc[i] = 0.0f;
 
   // A = -exp(A_log), 1/A and (fast path) A log2(e) for my states.
   float A[NPL], Ik[NPL];
@@ -454,44 +461,77 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
     __syncthreads();
 
     // recompute the chunk's states: hist[t + 1] = state after step t0 + t
+    // (The operands of the next step are loaded one step ahead: the stores
+    // and shared atomics of a step would otherwise hold back the next step's
+    // loads, which the compiler cannot prove independent.)
     load_state(cks);
     hist[tid] = state4();
-#pragma unroll 4
-    for (int t = 0; t < tv; ++t) {
-      const float4 tc = f_tc[t * CB + c];
-      fwd_step(ld4(f_B + t * N + n0), tc.x, tc.y);
-      hist[(t + 1) * kBwdThreads + tid] = state4();
+    {
+      float4 tc = f_tc[c], B4 = ld4(f_B + n0);
+#pragma unroll 2
+      for (int t = 0; t < tv; ++t) {
+        const int tn = t + 1 < tv ? t + 1 : t;
+        const float4 tc_n = f_tc[tn * CB + c], B4_n = ld4(f_B + tn * N + n0);
+        fwd_step(B4, tc.x, tc.y);
+        hist[(t + 1) * kBwdThreads + tid] = state4();
+        tc = tc_n;
+        B4 = B4_n;
+      }
     }
 
-    // adjoint, backwards through the chunk
+    // adjoint, backwards through the chunk, G::SBT steps per round of reductions
+    constexpr int SBT = G::SBT, VPL = G::VPL;
     float4 sn = state4();  // state after the chunk's last valid step
-    for (int t = tv - 1; t >= 0; --t) {
-      const float4 tc = f_tc[t * CB + c];
-      const float4 sp = hist[t * kBwdThreads + tid];
-      const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
-      float v[8], dus, ddt, ys;
-      if constexpr (PRECISE) adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
-      else adj_step_fast<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, Al2, Ik2, v, dus, ddt, ys);
-      sn = sp;
-      // (du, dt, y) sums over the channel's LPC lanes: lane part & 3 keeps one of them
-      {
-        float w[4] = {dus, ddt, ys, 0.0f};
-        reduce_scatter<4>(w, lane, 2);
-        reduce_scatter<2>(w, lane, 1);
+    for (int tb = tv - 1; tb >= 0; tb -= SBT) {
+      float vv[SBT * 8];  // per step: dB partials (states n0..n0+3), then dC partials
+      float ww[4 * SBT];  // [quantity][step]: du, dt and y sums over my states, 0
 #pragma unroll
-        for (int o = 4; o < LPC; o <<= 1) w[0] += __shfl_xor_sync(0xffffffffu, w[0], o);
-        if (part < 3) red[part * K * CB + t * CB + c] = w[0];
+      for (int si = 0; si < SBT; ++si) {
+        const int t = tb - si;
+        float v[8], dus = 0.0f, ddt = 0.0f, ys = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        if (t >= 0) {  // uniform across the CTA
+          const float4 tc = f_tc[t * CB + c];
+          const float4 sp = hist[t * kBwdThreads + tid];
+          const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
+          if constexpr (PRECISE)
+            adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
+          else
+            adj_step_fast<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, Al2, Ik2, v, dus, ddt, ys);
+          sn = sp;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vv[si * 8 + i] = v[i];
+        ww[si] = dus;
+        ww[SBT + si] = ddt;
+        ww[2 * SBT + si] = ys;
+        ww[3 * SBT + si] = 0.0f;
       }
-      // dB, dC summed over the channels of this warp (lane bits >= LPC)
-      int jh = 0;
-      if constexpr (LPC <= 16) { reduce_scatter<8>(v, lane, 16); jh = (lane >> 4) & 1; }
-      if constexpr (LPC <= 8) { reduce_scatter<4>(v, lane, 8); jh = jh * 2 + ((lane >> 3) & 1); }
-      if constexpr (LPC <= 4) { reduce_scatter<2>(v, lane, 4); jh = jh * 2 + ((lane >> 2) & 1); }
-      constexpr int W = (LPC <= 4) ? 1 : (LPC <= 8 ? 2 : (LPC <= 16 ? 4 : 8));
+      // (du, dt, y) sums over the channel's LPC lanes: lane part & 3 keeps quantity part & 3
+      reduce_scatter<4 * SBT>(ww, lane, 2);
+      reduce_scatter<2 * SBT>(ww, lane, 1);
 #pragma unroll
-      for (int i = 0; i < W; ++i) {
-        const int j = jh * W + i;  // 0..3: dB of state n0 + j; 4..7: dC of state n0 + j - 4
-        atomicAdd(&acc[t * 2 * N + (j >> 2) * N + n0 + (j & 3)], v[i]);
+      for (int o = 4; o < LPC; o <<= 1)
+#pragma unroll
+        for (int si = 0; si < SBT; ++si) ww[si] += __shfl_xor_sync(0xffffffffu, ww[si], o);
+      if (part < 3) {
+#pragma unroll
+        for (int si = 0; si < SBT; ++si)
+          if (tb - si >= 0) red[part * K * CB + (tb - si) * CB + c] = ww[si];
+      }
+      // dB, dC summed over the channels of this warp (lane bits >= LPC), highest bit first
+      int jh = 0;
+      if constexpr (G::R >= 1) { reduce_scatter<8 * SBT>(vv, lane, 16); jh = (lane >> 4) & 1; }
+      if constexpr (G::R >= 2) { reduce_scatter<4 * SBT>(vv, lane, 8); jh = jh * 2 + ((lane >> 3) & 1); }
+      if constexpr (G::R >= 3) { reduce_scatter<2 * SBT>(vv, lane, 4); jh = jh * 2 + ((lane >> 2) & 1); }
+#pragma unroll
+      for (int g = 0; g < VPL / 4; ++g) {
+        const int j0 = jh * VPL + 4 * g;  // index of (step, dB|dC, state n0) in vv
+        const int t = tb - (j0 >> 3);
+        if (t >= 0)
+          st4(acc + ((tid >> 5) * K + t) * 2 * N + ((j0 >> 2) & 1) * N + n0,
+              make_float4(vv[4 * g], vv[4 * g + 1], vv[4 * g + 2], vv[4 * g + 3]));
       }
     }
     __syncthreads();
@@ -507,13 +547,16 @@ __global__ void __launch_bounds__(kBwdThreads) scan_bwd_kernel(const BwdArgs a) 
       dD_acc = fmaf(tc.z, tc.y, dD_acc);
       dbias_acc += dd;
     }
-    for (int i = tid * 4; i < K * 2 * N; i += kBwdThreads * 4) {
+    for (int i = tid * 4; i < tv * 2 * N; i += kBwdThreads * 4) {
       const int t = i / (2 * N), j = i - t * 2 * N;
-      if (t < tv) {
-        float* dst = (j < N ? a.dB : a.dC) + (rowb + t0 + t) * N + (j < N ? j : j - N);
-        atomicAdd(reinterpret_cast<float4*>(dst), *reinterpret_cast<const float4*>(acc + i));
+      float4 sum = ld4(acc + i);
+#pragma unroll
+      for (int w = 1; w < G::NW; ++w) {
+        const float4 x = ld4(acc + w * K * 2 * N + i);
+        sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
       }
-      st4(acc + i, zero4);
+      float* dst = (j < N ? a.dB : a.dC) + (rowb + t0 + t) * N + (j < N ? j : j - N);
+      atomicAdd(reinterpret_cast<float4*>(dst), sum);
     }
     __syncthreads();
     OCopy3::smem_to_global(sm + G::oO, dst_o, rowb + t0, Dm, d0, nch, tv, tid);
