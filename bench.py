@@ -511,10 +511,10 @@ def oracle_sample_rate(cfg, inp, seconds, threads):
         dt = run(k)
     per_ch = dt / k
     k_final = max(1, min(Dm, int(seconds / per_ch)))
-    reps = max(1, int(seconds / (per_ch * k_final)))
-    total = 0.0
-    for _ in range(reps):
+    total, reps = 0.0, 0
+    while total < seconds:  # whole calls until the time budget is spent
         total += run(k_final)
+        reps += 1
     rate = reps * k_final * L / total
     return rate, f"oracle scan of {k_final} channels x {L} steps (batch row 0) x {reps}, {total:.1f} s"
 
