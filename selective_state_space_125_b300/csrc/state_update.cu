@@ -214,13 +214,13 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
 // ---------------------------------------------------------------------------
 // Bulk-staged decode step for the common layouts (N % 8 == 0, N <= 256,
 // dim % 8 == 0, 16-byte aligned pointers). A CTA owns a block of channels
-// and walks batch rows. For every row a 4-stage ring in shared memory receives,
+// and walks batch rows. For every row a 4- or 8-stage ring in shared memory receives,
 // by bulk copies that complete on an mbarrier, the row's state slab (8 KB)
 // and its u, delta, z, B, C. The threads update the slab in place (8 states
 // each), and one thread writes it back with a bulk store. Each thread
-// computes A and 1/A for its states once. The loads of rows i + 1 .. i + 7
-// are in flight while row i is computed, so the kernel keeps many bytes in
-// flight without registers.
+// computes A and 1/A for its states once. With an S-stage ring the loads of
+// rows i + 1 .. i + S - 1 are in flight while row i is computed, so the kernel
+// keeps many bytes in flight without registers.
 
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -240,12 +240,12 @@ __device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 constexpr int kBulkThreads = 256;
-constexpr int kBulkStages = 8;
 constexpr int kBulkFloats = 8;  // states per thread
 
-// Shared-memory layout of one stage (8 stages, about 68 KB per CTA): state
-// slab, then u, delta, z, B, C.
-template <typename Tin, int TPC>
+// Shared-memory layout of one of the S stages (about 8.6 KB each: the slab is
+// always 256 / TPC channels x 8 TPC states x 4 bytes = 8 KB): state slab, then
+// u, delta, z, B, C.
+template <typename Tin, int TPC, int S>
 struct BulkGeom {
   static constexpr int kN = TPC * kBulkFloats;  // state size this variant serves
   static constexpr int kCBD = kBulkThreads / TPC;  // channels per block
@@ -253,7 +253,7 @@ struct BulkGeom {
   static constexpr size_t kVec = (size_t(kCBD) * sizeof(Tin) + 15) & ~size_t(15);
   static constexpr size_t kBC = (size_t(kN) * sizeof(Tin) + 15) & ~size_t(15);
   static constexpr size_t kStage = kState + 3 * kVec + 2 * kBC;
-  static constexpr size_t kSmem = kBulkStages * kStage + 64 + 128;
+  static constexpr size_t kSmem = S * kStage + 8 * S + 128;
 };
 
 // Eight consecutive B or C values of one row, from shared memory, as fp32.
@@ -272,12 +272,12 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <typename Tin, int TPC, int DISC>
+template <typename Tin, int TPC, int DISC, int S>
 __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const DecodeArgs a) {
-  using G = BulkGeom<Tin, TPC>;
+  using G = BulkGeom<Tin, TPC, S>;
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
-  constexpr int N = G::kN, CBD = G::kCBD, S = kBulkStages;
+  constexpr int N = G::kN, CBD = G::kCBD;
   extern __shared__ unsigned char smem_dyn[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
@@ -439,23 +439,34 @@ static bool decode_bulk_ok(const DecodeArgs& a) {
          al16(a.delta) && (!a.z || al16(a.z)) && al16(a.B) && al16(a.C);
 }
 
-template <typename Tin, int TPC, int DISC>
-static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
-  using G = BulkGeom<Tin, TPC>;
+template <typename Tin, int TPC, int DISC, int S>
+static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, cudaStream_t stream) {
+  using G = BulkGeom<Tin, TPC, S>;
   static bool configured = false;  // per instantiation; benign race (idempotent)
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(state_update_bulk_kernel<Tin, TPC, DISC>,
+    cudaError_t e = cudaFuncSetAttribute(state_update_bulk_kernel<Tin, TPC, DISC, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + G::kCBD - 1) / G::kCBD;
-  // row groups for about 8 CTAs per SM (3 resident at a time with 8 stages): shorter
-  // CTAs measured faster than fewer, longer ones on B300
-  const int rb = std::max(1, std::min(a.batch, (8 * sms + blocks_x - 1) / blocks_x));
-  state_update_bulk_kernel<Tin, TPC, DISC><<<dim3(blocks_x, rb), kBulkThreads, G::kSmem, stream>>>(a);
+  const int rb = std::max(1, std::min(a.batch, (ctas_per_sm * sms + blocks_x - 1) / blocks_x));
+  state_update_bulk_kernel<Tin, TPC, DISC, S><<<dim3(blocks_x, rb), kBulkThreads, G::kSmem, stream>>>(a);
   return cudaGetLastError();
+}
+
+// Ring depth and grid, from sweeps on B300 (batch 128, dim 5120): with few
+// channel blocks (small N) every CTA walks only a few rows, and a 4-stage ring
+// that fits 6 CTAs per SM is best (N = 16: 20.5 us against 22.5 us with 8
+// stages); with many channel blocks (large N) an 8-stage ring over about 11
+// rows per CTA is best (N = 128: 123 us against 129 us with 32 rows per CTA).
+template <typename Tin, int TPC, int DISC>
+static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
+  const int sms = a.sms > 0 ? a.sms : 148;
+  const int blocks_x = (a.dim + BulkGeom<Tin, TPC, 8>::kCBD - 1) / BulkGeom<Tin, TPC, 8>::kCBD;
+  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4>(a, 8, stream);
+  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8>(a, 24, stream);
 }
 
 template <typename Tin, int TPC>
