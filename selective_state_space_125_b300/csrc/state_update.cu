@@ -439,34 +439,43 @@ static bool decode_bulk_ok(const DecodeArgs& a) {
          al16(a.delta) && (!a.z || al16(a.z)) && al16(a.B) && al16(a.C);
 }
 
+// one_wave: as many row groups as fill every SM once at the kernel's
+// occupancy; otherwise enough row groups for about ctas_per_sm CTAs per SM.
 template <typename Tin, int TPC, int DISC, int S>
-static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, cudaStream_t stream) {
+static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, bool one_wave, int ctas_per_sm, cudaStream_t stream) {
   using G = BulkGeom<Tin, TPC, S>;
-  static bool configured = false;  // per instantiation; benign race (idempotent)
-  if (!configured) {
+  static int occupancy = 0;  // per instantiation; benign race (idempotent)
+  if (occupancy == 0) {
     cudaError_t e = cudaFuncSetAttribute(state_update_bulk_kernel<Tin, TPC, DISC, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
+    int occ = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, state_update_bulk_kernel<Tin, TPC, DISC, S>,
+                                                        kBulkThreads, G::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    occupancy = std::max(1, occ);
   }
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + G::kCBD - 1) / G::kCBD;
-  const int rb = std::max(1, std::min(a.batch, (ctas_per_sm * sms + blocks_x - 1) / blocks_x));
+  const int groups = one_wave ? occupancy * sms / blocks_x : (ctas_per_sm * sms + blocks_x - 1) / blocks_x;
+  const int rb = std::max(1, std::min(a.batch, groups));
   state_update_bulk_kernel<Tin, TPC, DISC, S><<<dim3(blocks_x, rb), kBulkThreads, G::kSmem, stream>>>(a);
   return cudaGetLastError();
 }
 
-// Ring depth and grid, from sweeps on B300 (batch 128, dim 5120): with few
-// channel blocks (small N) every CTA walks only a few rows, and a 4-stage ring
-// that fits 6 CTAs per SM is best (N = 16: 20.5 us against 22.5 us with 8
-// stages); with many channel blocks (large N) an 8-stage ring over about 11
-// rows per CTA is best (N = 128: 123 us against 129 us with 32 rows per CTA).
+// Ring depth and grid, from sweeps on B300 (batch 128, dim 5120, 3-12 stages,
+// 3-32 CTAs per SM):
+// - with few channel blocks (small N), a 4-stage ring and exactly one wave of
+//   CTAs, each walking batch / row-groups rows (N = 16: 18.5 us, against 20.5 us
+//   with 2.7 waves of 4-row CTAs and 22.5 us with 8 stages);
+// - with many channel blocks (large N), an 8-stage ring over about 11 rows per
+//   CTA (N = 128: 123 us, against 129 us with 32 rows per CTA).
 template <typename Tin, int TPC, int DISC>
 static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + BulkGeom<Tin, TPC, 8>::kCBD - 1) / BulkGeom<Tin, TPC, 8>::kCBD;
-  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4>(a, 8, stream);
-  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8>(a, 24, stream);
+  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4>(a, true, 0, stream);
+  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8>(a, false, 24, stream);
 }
 
 template <typename Tin, int TPC>
