@@ -180,3 +180,36 @@ def test_bwd_repeatable_up_to_atomics():
         assert np.array_equal(g1[k], g2[k]), k
     for k in ("dB", "dC", "dA_log", "dD", "ddelta_bias"):
         assert parity_err(g1[k], g2[k]) < 1e-5, k
+
+
+def test_bwd_under_cuda_graph_capture():
+    """The call allocates its checkpoint workspace with cudaMallocAsync on the stream; captured
+    in a CUDA graph and replayed, it gives the eager call's gradients."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    dev = dev_holder["dev"]
+    inp = make_bwd_inputs(2, 64, 16, 70, "bf16", 9)
+    dt = inp["dtype"]
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    args = (to_torch(inp["u"], dt, dev), to_torch(inp["delta"], dt, dev), f32(inp["A_log"]),
+            to_torch(inp["B"], dt, dev), to_torch(inp["C"], dt, dev), to_torch(inp["dout"], dt, dev))
+    kw = dict(D=f32(inp["D"]), z=to_torch(inp["z"], dt, dev), delta_bias=f32(inp["delta_bias"]))
+    eager = binding.mamba_selective_scan_bwd(*args, **kw)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        binding.mamba_selective_scan_bwd(*args, **kw)  # warm-up on the capture stream
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        captured = binding.mamba_selective_scan_bwd(*args, **kw)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    for k in ("du", "ddelta", "dz"):
+        assert torch.equal(eager[k], captured[k]), k
+    for k in ("dA_log", "dB", "dC", "dD", "ddelta_bias"):
+        assert parity_err(to_numpy(captured[k]), to_numpy(eager[k])) < 1e-5, k

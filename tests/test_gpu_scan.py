@@ -273,3 +273,31 @@ def test_conv_scan_m130_sampled(dev):
                                         inp["D"][ds], sub["z"], inp["delta_bias"][ds])
     assert parity_err(out[bs][:, :, ds], rout) <= TOL["bf16"]
     assert parity_err(last[bs][:, ds], rlast) <= TOL["bf16"]
+
+
+def test_segmented_scan_under_cuda_graph_capture(dev):
+    """A plan with time segments allocates its aggregate workspace with cudaMallocAsync; captured
+    in a CUDA graph and replayed, it matches the eager call bit for bit."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    inp = make_scan_inputs(2, 64, 16, 300, "bf16", seed=31)
+    t = upload_scan(inp, dev)
+    plan = binding.ScanPlan(1, 3, 0, 0)
+    eager, eager_last = binding.mamba_selective_scan_fwd(t["u"], t["delta"], t["A_log"], t["B"], t["C"], t["D"],
+                                                         t["z"], t["delta_bias"], return_last_state=True, plan=plan)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        binding.mamba_selective_scan_fwd(t["u"], t["delta"], t["A_log"], t["B"], t["C"], t["D"], t["z"],
+                                         t["delta_bias"], return_last_state=True, plan=plan)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out, last = binding.mamba_selective_scan_fwd(t["u"], t["delta"], t["A_log"], t["B"], t["C"], t["D"],
+                                                     t["z"], t["delta_bias"], return_last_state=True, plan=plan)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    assert torch.equal(out, eager) and torch.equal(last, eager_last)
