@@ -478,8 +478,9 @@ def run_ours(args, rank, world, device):
     result = {
         "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded numpy, see DESIGN.md)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy, see DESIGN.md)",
         "config": {"workload": cfg.description, "batch": B, "d_inner": Dm, "d_state": N, "seqlen": L,
+                   "input_dtype": cfg.dtype, "state_dtype": "f32",
                    "step": "scan(L tokens, last_state) + 1 decode step", "channel_steps_per_step": chsteps,
                    "l2": f"{nsets} rotating input/output sets of {set_bytes / 2**20:.0f} MiB (> L2)",
                    "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
