@@ -215,11 +215,16 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[LPC], int q) {
   return v[0];
 }
 
-// CTAs per SM each variant's register budget is sized for: 8 (<= 64
-// registers) with 4 states per thread, 7 (<= 72) with 8, 4 (<= 128) with 16.
+// CTAs per SM each variant's register budget is sized for: 4 (<= 128
+// registers per thread) for every state split. The scans these plans serve are
+// latency-bound at a few CTAs per SM, and the registers let the compiler move a
+// step group's softplus, loads and exponentials ahead of the state chain. On
+// B300 the 4-state variant on the 130M-shaped layer (2.6 CTAs per SM) went from
+// 277 us at 8 CTAs per SM (64 registers) to 239 us; 5 and 6 gave 251 and 265 us,
+// and a layer with 7 CTAs per SM ran the same with either budget.
 template <int NPL>
 struct ScanMinBlocks {
-  static constexpr int value = NPL <= 4 ? 8 : (NPL <= 8 ? 7 : 4);
+  static constexpr int value = 4;
 };
 
 // DISC: 0 = zero-order hold (the method), 1 = simplified Bbar = dt B.
