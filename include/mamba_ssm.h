@@ -281,11 +281,12 @@ MAMBA_API mamba_status_t mamba_selective_state_update_ex(
  * (MAMBA_ERR_UNSUPPORTED otherwise). Outputs may not alias inputs or each
  * other (MAMBA_ERR_INVALID_ARG).
  *
- * Work: the call zeroes dA_log, dB, dC, dD, ddelta_bias on `stream`, then one
+ * Work: the call zeroes dA_log, dB, dC, dD, ddelta_bias on `stream`, then a
  * kernel launch runs the forward over each channel, stores the state every 16
  * steps in a stream-ordered workspace of B * ceil(L/16) * D * N * 4 bytes
  * (cudaMallocAsync / cudaFreeAsync on `stream`), and walks the chunks
- * backwards. dB, dC, dA_log, dD and ddelta_bias are sums over channels or
+ * backwards. When few channel blocks x batch rows would leave SMs idle, the
+ * sequence is cut into time segments (see mamba_selective_scan_bwd_ex). dB, dC, dA_log, dD and ddelta_bias are sums over channels or
  * batch rows taken with fp32 atomics, so their last bits may differ from call
  * to call. MAMBA_F32 inputs use expf / expm1f; MAMBA_BF16 inputs use the
  * hardware ex2 / rcp approximations, as the forward does.
@@ -297,6 +298,25 @@ MAMBA_API mamba_status_t mamba_selective_scan_bwd(
     const void *dout, const float *dlast_state,
     void *du, void *ddelta, float *dA_log, float *dB, float *dC,
     float *dD, void *dz, float *ddelta_bias, float *dinitial_state, mamba_stream_t stream);
+
+/*
+ * As mamba_selective_scan_bwd, with the number of time segments: 0 chooses
+ * automatically (segments only when the channel blocks x batch rows leave SMs
+ * idle), 1 runs each channel over the whole sequence, k > 1 cuts the sequence
+ * into about k segments of whole 16-step chunks (at most 64). With segments, two
+ * extra launches precede the gradient pass: each segment's end state from a zero
+ * start, and the adjoint each segment passes back from a zero adjoint; the
+ * gradient pass composes them per segment (the split-sequence carry of the
+ * forward, run forward and backward in time). The workspace grows by
+ * B * segments * D * (2 N + 1) * 4 bytes. segments < 0: MAMBA_ERR_INVALID_ARG.
+ */
+MAMBA_API mamba_status_t mamba_selective_scan_bwd_ex(
+    int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, int discretization,
+    const void *u, const void *delta, const float *A_log, const void *B, const void *C,
+    const float *D, const void *z, const float *delta_bias, const float *initial_state,
+    const void *dout, const float *dlast_state,
+    void *du, void *ddelta, float *dA_log, float *dB, float *dC,
+    float *dD, void *dz, float *ddelta_bias, float *dinitial_state, int segments, mamba_stream_t stream);
 
 /* Static description of a status code. */
 MAMBA_API const char *mamba_status_string(mamba_status_t s);

@@ -29,7 +29,7 @@ EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
             "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_state_update_ex", "mamba_conv1d_selective_scan_fwd",
-            "mamba_selective_scan_bwd")
+            "mamba_selective_scan_bwd", "mamba_selective_scan_bwd_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def library() -> ctypes.CDLL:
             lib.mamba_conv1d_selective_scan_fwd.restype = i
             lib.mamba_selective_scan_bwd.argtypes = [i, i, i, i, i, i] + [vp] * 20 + [vp]
             lib.mamba_selective_scan_bwd.restype = i
+            lib.mamba_selective_scan_bwd_ex.argtypes = [i, i, i, i, i, i] + [vp] * 20 + [i, vp]
+            lib.mamba_selective_scan_bwd_ex.restype = i
             lib.mamba_status_string.argtypes = [i]
             lib.mamba_status_string.restype = ctypes.c_char_p
             lib.mamba_last_error_detail.argtypes = []
@@ -186,7 +188,8 @@ def mamba_selective_scan_fwd(u, delta, A_log, B, C, D=None, z=None, delta_bias=N
 
 def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_bias=None,
                              initial_state=None, dlast_state=None, *, discretization=MAMBA_ZOH,
-                             need_dD=None, need_ddelta_bias=None, need_dinitial_state=None, stream=None):
+                             need_dD=None, need_ddelta_bias=None, need_dinitial_state=None, segments=None,
+                             stream=None):
     """Gradients of sum(dout * out) + sum(dlast_state * last_state) through the C ABI.
 
     Inputs as for ``mamba_selective_scan_fwd``; dout is like u and dlast_state
@@ -194,7 +197,8 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
     (like u, or None without z), dA_log (dim, N), dB, dC (batch, L, N) float32,
     and dD, ddelta_bias (dim,), dinitial_state (batch, dim, N) float32 -- each
     computed when the matching input is given or its ``need_*`` flag is set,
-    else None.
+    else None. ``segments`` (None or 0: automatic, 1: none, k: about k time
+    segments) goes to mamba_selective_scan_bwd_ex.
     """
     torch = _torch()
     batch, seqlen, dim = u.shape
@@ -214,7 +218,10 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
          "dinitial_state": (torch.empty((batch, dim, dstate), **f32)
                             if want(need_dinitial_state, initial_state is not None) else None)}
     st = (batch, dim, dstate)
-    check(library().mamba_selective_scan_bwd(
+    lib = library()
+    fn = lib.mamba_selective_scan_bwd if segments is None else lib.mamba_selective_scan_bwd_ex
+    extra = () if segments is None else (int(segments),)
+    check(fn(
         batch, dim, dstate, seqlen, code, int(discretization),
         _ptr(u, "u", xs, u.dtype, dev), _ptr(delta, "delta", xs, u.dtype, dev),
         _ptr(A_log, "A_log", (dim, dstate), torch.float32, dev),
@@ -226,7 +233,7 @@ def mamba_selective_scan_bwd(u, delta, A_log, B, C, dout, D=None, z=None, delta_
         _ptr(g["du"], "du"), _ptr(g["ddelta"], "ddelta"), _ptr(g["dA_log"], "dA_log"),
         _ptr(g["dB"], "dB"), _ptr(g["dC"], "dC"), _ptr(g["dD"], "dD"), _ptr(g["dz"], "dz"),
         _ptr(g["ddelta_bias"], "ddelta_bias"), _ptr(g["dinitial_state"], "dinitial_state"),
-        _stream(stream, dev)))
+        *extra, _stream(stream, dev)))
     return g
 
 

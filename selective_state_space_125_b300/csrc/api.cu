@@ -492,14 +492,15 @@ mamba_status_t mamba_selective_state_update(int batch, int dim, int dstate, mamb
                                          delta_bias, out, 0, stream);
 }
 
-mamba_status_t mamba_selective_scan_bwd(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
-                                        int discretization, const void* u, const void* delta, const float* A_log,
-                                        const void* B, const void* C, const float* D, const void* z,
-                                        const float* delta_bias, const float* initial_state, const void* dout,
-                                        const float* dlast_state, void* du, void* ddelta, float* dA_log, float* dB,
-                                        float* dC, float* dD, void* dz, float* ddelta_bias, float* dinitial_state,
-                                        mamba_stream_t stream_) {
+mamba_status_t mamba_selective_scan_bwd_ex(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                           int discretization, const void* u, const void* delta, const float* A_log,
+                                           const void* B, const void* C, const float* D, const void* z,
+                                           const float* delta_bias, const float* initial_state, const void* dout,
+                                           const float* dlast_state, void* du, void* ddelta, float* dA_log, float* dB,
+                                           float* dC, float* dD, void* dz, float* ddelta_bias,
+                                           float* dinitial_state, int segments, mamba_stream_t stream_) {
   t_detail.clear();
+  if (segments < 0) return fail(MAMBA_ERR_INVALID_ARG, "segments=%d must be >= 0 (0 = automatic)", segments);
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 0 || dim < 0 || seqlen < 0)
     return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
@@ -596,16 +597,55 @@ mamba_status_t mamba_selective_scan_bwd(int batch, int dim, int dstate, int seql
   a.dh0 = dinitial_state;
   a.disc = discretization;
   a.aligned = aligned ? 1 : 0;
-  const size_t ck_bytes = (size_t)batch * a.nchunk * dim * dstate * sizeof(float);
+
+  // Time segments: when the channel blocks x batch rows leave SMs idle, cut the sequence
+  // into segments of whole chunks so that about 12 CTAs per SM are launched, keeping at
+  // least 4 chunks per segment. On B300 (B1 D5120 N16 L32768, bf16) 1, 2, 5, 11 and 32
+  // segments took 12.97, 10.85, 8.87, 8.11 and 8.18 ms; past about 8 the kernel runs at
+  // the throughput of a full GPU and the two segment passes take the rest.
+  DeviceInfo di;
+  mamba_status_t st = device_info(&di);
+  if (st != MAMBA_OK) return st;
+  int nseg = segments;
+  if (nseg == 0) {
+    const long ctas = (long)((dim + cb - 1) / cb) * batch;
+    nseg = 1;
+    if (ctas < 2L * di.sms) nseg = int(std::min<long>(12L * di.sms / ctas, a.nchunk / 4));
+  }
+  nseg = std::max(1, std::min({nseg, kBwdMaxSegments, a.nchunk}));
+  const int chunks_per_seg = (a.nchunk + nseg - 1) / nseg;
+  a.seg_len = chunks_per_seg * kBwdChunk;
+  a.nseg = (seqlen + a.seg_len - 1) / a.seg_len;
+
+  const size_t ck_elems = (size_t)batch * a.nchunk * dim * dstate;
+  const size_t seg_state = a.nseg > 1 ? (size_t)batch * a.nseg * dim * dstate : 0;
+  const size_t seg_vec = a.nseg > 1 ? (size_t)batch * a.nseg * dim : 0;
   void* ck = nullptr;
-  e = cudaMallocAsync(&ck, ck_bytes, stream);
+  e = cudaMallocAsync(&ck, (ck_elems + 2 * seg_state + seg_vec) * sizeof(float), stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(backward checkpoint workspace)");
   a.ck = static_cast<float*>(ck);
+  if (a.nseg > 1) {
+    a.seg_h = a.ck + ck_elems;
+    a.seg_g = a.seg_h + seg_state;
+    a.seg_dsum = a.seg_g + seg_state;
+  }
   e = launch_scan_bwd(dtype, a, stream);
   cudaError_t e2 = cudaFreeAsync(ck, stream);
   if (e != cudaSuccess) return cuda_fail(e, "backward scan launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync(backward checkpoint workspace)");
   return MAMBA_OK;
+}
+
+mamba_status_t mamba_selective_scan_bwd(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype,
+                                        int discretization, const void* u, const void* delta, const float* A_log,
+                                        const void* B, const void* C, const float* D, const void* z,
+                                        const float* delta_bias, const float* initial_state, const void* dout,
+                                        const float* dlast_state, void* du, void* ddelta, float* dA_log, float* dB,
+                                        float* dC, float* dD, void* dz, float* ddelta_bias, float* dinitial_state,
+                                        mamba_stream_t stream) {
+  return mamba_selective_scan_bwd_ex(batch, dim, dstate, seqlen, in_dtype, discretization, u, delta, A_log, B, C, D,
+                                     z, delta_bias, initial_state, dout, dlast_state, du, ddelta, dA_log, dB, dC, dD,
+                                     dz, ddelta_bias, dinitial_state, 0, stream);
 }
 
 const char* mamba_status_string(mamba_status_t s) {

@@ -1,0 +1,712 @@
+// Backward of the selective scan: the gradients of
+//   loss = sum_{b,t,d} dout * out + sum_{b,d,n} dlast * last_state
+// with respect to u, delta, A_log, B, C, D, z, delta_bias and the initial
+// state, for the recurrence of "State Space Models and Mamba" §2-§4 (zero-order
+// hold, or the simplified Bbar = dt B) with the D skip and SiLU gate of the
+// "Mamba" paper notes (selective_ssm sketch, Overall framework).
+//
+// Work layout: a CTA owns CB channels of one batch row; LPC = N / 4 threads
+// share a channel, 4 states each. Phase 1 runs the forward recurrence over the
+// sequence and writes the state at the start of every 16-step chunk to a
+// workspace; each thread reads back only the slots it wrote. Phase 2 walks the
+// chunks backwards. For each chunk it stages the tiles (u, delta, z, dout, B,
+// C) in shared memory, recomputes the chunk's states from its checkpoint into
+// a per-thread shared-memory history, and runs the adjoint recurrence
+//   lambda_t = dy_t C_t + abar_{t+1} lambda_{t+1}    (lambda = dloss / dh_t)
+// backwards through the chunk. The tiles of the next chunk are loaded into
+// registers while the current one is computed.
+//
+// Per step and state, with abar = exp(dt A), q = (abar - 1) / A (zero-order
+// hold) or dt (simplified), and v = A h_{t-1} + B u:
+//   dloss/d dt    += abar lambda v                    (simplified: lambda (abar A h_{t-1} + B u))
+//   dloss/d A_log += dt abar lambda v - q lambda B u   (simplified: dt abar lambda A h_{t-1})
+//   dloss/d B_n   += lambda q u,   dloss/d u += lambda q B_n,   dloss/d C_n += dy h_t
+// (dA_log = A dA because A = -exp(A_log).) The sums over states of the dt and
+// u terms are reduced across the LPC threads of a channel with shuffles; the
+// sums of dB and dC over channels are reduce-scattered across the channels of
+// a warp, summed across warps in shared memory and once per chunk into global
+// memory. The reduce-scatters run over several steps at once, so that their
+// shuffle latency is paid once per group of steps. Per-channel sums over the
+// batch (dA_log, dD, ddelta_bias) are added with one atomic per thread at the end.
+//
+// Math: bf16 inputs use MUFU ex2/rcp and keep the scaled state s = A h during
+// the recomputation (s_t = abar (s_{t-1} + B u) - B u, so A h_{t-1} is read
+// directly); fp32 inputs use expm1f and the unscaled h, as the forward does.
+//
+// Time segments (for small batch x channels over long sequences): the
+// sequence is cut into S segments of whole chunks, one CTA per (channel
+// block, batch row, segment). Two cheap passes run first. The forward
+// aggregate gives each segment's end state from h = 0 and its sum of dt; the
+// adjoint aggregate gives the carry each segment passes to its left when zero
+// enters it from the right (it needs only dt, A, dy and C: lambda_t = dy_t C_t
+// + abar_{t+1} lambda_{t+1} is linear in lambda). The full pass then composes,
+// per segment k, the state entering it (h0 through segments 0..k-1, each
+// decaying by exp(A sum dt)) and the adjoint entering it from the right
+// (dlast through segments S-1..k+1), and runs as above over its own chunks.
+// This is the forward's split-L carry ("State Space Models and Mamba" §4,
+// parallel scan), applied once forward and once backward in time.
+#pragma once
+
+#include <type_traits>
+
+#include "bwd_args.h"
+#include "device_common.cuh"
+
+namespace mamba {
+namespace {
+
+template <int SB> struct RawOf;
+template <> struct RawOf<16> { using type = uint4; };
+template <> struct RawOf<8> { using type = uint2; };
+template <> struct RawOf<4> { using type = unsigned int; };
+template <> struct RawOf<2> { using type = unsigned short; };
+
+constexpr size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__device__ __forceinline__ float sigmoid_fast(float x) { return hw_rcp(1.0f + hw_ex2(-x * kLog2e)); }
+__device__ __forceinline__ float sigmoid_precise(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+template <typename Tin, int N, bool ALIGNED>
+struct BwdGeom {
+  static constexpr int NPL = 4;
+  static constexpr int LPC = N / NPL;
+  static constexpr int CB = kBwdThreads / LPC;
+  static constexpr int K = kBwdChunk;
+  static constexpr int ES = int(sizeof(Tin));
+  static constexpr int SBX = ALIGNED ? (CB * ES < 16 ? CB * ES : 16) : ES;  // bytes per slot of a (t, d) tile
+  static constexpr int SBB = ALIGNED ? 16 : ES;                             // bytes per slot of a (t, n) tile
+  static constexpr size_t szX = size_t(K) * CB * ES;
+  static constexpr size_t szBC = size_t(K) * N * ES;
+  static constexpr size_t szF = size_t(K) * CB * 4;
+  static constexpr size_t oX = 0;                                      // raw u, delta, z, dout tiles
+  static constexpr size_t oBC = align16(oX + 4 * szX);                 // raw B, C tiles
+  static constexpr size_t oO = align16(oBC + 2 * szBC);                // raw du, ddelta, dz tiles
+  static constexpr size_t oTC = align16(oO + 3 * szX);                 // [K][CB] float4 (dt, u, dy, sigmoid)
+  static constexpr size_t oDz = oTC + 4 * szF;                         // [K][CB] dz factor
+  static constexpr size_t oRed = oDz + szF;                            // [3][K][CB] sums over states
+  static constexpr size_t oBf = oRed + 3 * szF;                        // B, C as float
+  static constexpr int NW = kBwdThreads / 32;
+  static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [warps][K][2N] dB | dC of the chunk
+  static constexpr size_t oCh = oAcc + size_t(NW) * K * 2 * N * 4;     // per-channel bias, D
+  static constexpr size_t oHist = align16(oCh + 2 * size_t(CB) * 4);   // [K+1][threads] states
+  static constexpr size_t kSmem = oHist + size_t(K + 1) * kBwdThreads * 16;
+  static_assert(N % 16 == 0 && LPC <= 32, "state size must be 16, 32, 64 or 128");
+  static_assert((CB * ES) % SBX == 0 && (N * ES) % SBB == 0, "slot width must divide a tile row");
+  static_assert(kBwdThreads % CB == 0, "a thread's epilogue channel is tid % CB");
+  // Reduce-scatters run over SBT steps at once: R = log2(channels per warp)
+  // rounds for dB/dC leave VPL values per lane (4, or 8 when a warp holds one
+  // channel); the (du, dt, y) sums take 2 rounds plus log2(LPC / 4) butterflies.
+  static constexpr int R = (LPC == 4) ? 3 : (LPC == 8 ? 2 : (LPC == 16 ? 1 : 0));
+  static constexpr int SBT = (R >= 2) ? (1 << R) / 2 : 1;
+  static constexpr int VPL = (8 * SBT) >> R;
+};
+
+// Copies of NT tiles of [K][W] elements between global memory and shared
+// memory in SB-byte slots. The slot space is tile-major, so slot s sits at
+// byte s * SB of the shared-memory tile area (each tile K * W * ES bytes).
+// Element (row, e) of tile `tile` is at base(tile) + (row0 + row) * stride +
+// col0 + e in global memory; rows >= nrows, columns >= ncols and null bases
+// are skipped (zero on load).
+template <int ES, int SB, int W, int K, int NT>
+struct TileCopy {
+  static constexpr int kRow = W * ES / SB;
+  static constexpr int kTile = K * kRow;
+  static constexpr int kTotal = NT * kTile;
+  static constexpr int kPer = (kTotal + kBwdThreads - 1) / kBwdThreads;
+  using Raw = typename RawOf<SB>::type;
+  Raw r[kPer];
+
+  template <class Src>
+  __device__ __forceinline__ void load(Src src, size_t row0, size_t stride, int col0, int ncols, int nrows,
+                                       int tid) {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int s = tid + j * kBwdThreads;
+      r[j] = Raw{};
+      if (s < kTotal) {
+        const int tile = s / kTile, rem = s - tile * kTile, row = rem / kRow, e = (rem - row * kRow) * (SB / ES);
+        const unsigned char* base = static_cast<const unsigned char*>(src(tile));
+        if (base != nullptr && row < nrows && e < ncols)
+          r[j] = *reinterpret_cast<const Raw*>(base + ((row0 + row) * stride + col0 + e) * ES);
+      }
+    }
+  }
+  __device__ __forceinline__ void to_smem(unsigned char* dst, int tid) const {
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int s = tid + j * kBwdThreads;
+      if (s < kTotal) *reinterpret_cast<Raw*>(dst + size_t(s) * SB) = r[j];
+    }
+  }
+  template <class Dst>
+  static __device__ __forceinline__ void smem_to_global(const unsigned char* srcsm, Dst dst, size_t row0,
+                                                        size_t stride, int col0, int ncols, int nrows, int tid) {
+    for (int s = tid; s < kTotal; s += kBwdThreads) {
+      const int tile = s / kTile, rem = s - tile * kTile, row = rem / kRow, e = (rem - row * kRow) * (SB / ES);
+      unsigned char* base = static_cast<unsigned char*>(dst(tile));
+      if (base != nullptr && row < nrows && e < ncols)
+        *reinterpret_cast<Raw*>(base + ((row0 + row) * stride + col0 + e) * ES) =
+            *reinterpret_cast<const Raw*>(srcsm + size_t(s) * SB);
+    }
+  }
+};
+
+// One round of a reduce-scatter across the lanes that differ in bit `m`: each
+// lane keeps half of its M values (the upper half if its bit is set), summed
+// with the partner's copy of that half.
+template <int M>
+__device__ __forceinline__ void reduce_scatter(float* v, int lane, int m) {
+  const bool up = (lane & m) != 0;
+#pragma unroll
+  for (int i = 0; i < M / 2; ++i) {
+    const float send = up ? v[i] : v[i + M / 2];
+    const float keep = up ? v[i + M / 2] : v[i];
+    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+  }
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float2 lo2(float4 v) { return make_float2(v.x, v.y); }
+__device__ __forceinline__ float2 hi2(float4 v) { return make_float2(v.z, v.w); }
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(hw_ex2(x.x), hw_ex2(x.y)); }
+
+// ---------------------------------------------------- forward step (4 states)
+// bf16 inputs: scaled state s = A h in two packed pairs; Al = A log2(e).
+template <int DISC>
+__device__ __forceinline__ void fwd_step_fast(float2 (&s)[2], float4 B4, float dt, float uu, const float2 (&Al)[2],
+                                              const float2 (&A)[2]) {
+  const float2 dd = dup2(dt), u2 = dup2(uu), nu = dup2(-uu);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
+    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    if (DISC == 0) {
+      s[h] = __ffma2_rn(ab, __ffma2_rn(Bp, u2, s[h]), __fmul2_rn(Bp, nu));  // abar (s + B u) - B u
+    } else {
+      s[h] = __ffma2_rn(ab, s[h], __fmul2_rn(__fmul2_rn(A[h], dd), __fmul2_rn(Bp, u2)));  // abar s + A dt B u
+    }
+  }
+}
+
+// fp32 inputs: h itself, expm1f.
+template <int DISC>
+__device__ __forceinline__ void fwd_step_precise(float (&h)[4], float4 B4, float dt, float uu, const float (&A)[4],
+                                                 const float (&Ik)[4]) {
+  const float Bv[4] = {B4.x, B4.y, B4.z, B4.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float e = expm1f(dt * A[k]);
+    const float q = DISC ? dt : e * Ik[k];
+    h[k] = fmaf(e, h[k], fmaf(q, Bv[k] * uu, h[k]));  // (1 + e) h + q B u
+  }
+}
+
+// ---------------------------------------------------- adjoint step (4 states)
+// Given s_t (sn), s_{t-1} (sp) and lambda_{t+1} abar_{t+1} (carry): updates
+// carry to abar_t lambda_t, adds the dA_log terms, writes the dB partials to
+// v[0..3] and the dC partials to v[4..7], and returns the sums over the 4
+// states of the du, dt and y terms.
+template <int DISC>
+__device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, float4 C4, float dt, float uu, float dy,
+                                              float2 (&carry)[2], float2 (&dApos)[2], float2 (&dAneg)[2],
+                                              const float2 (&Al)[2], const float2 (&Ik)[2], float (&v)[8],
+                                              float& dus, float& ddt, float& ys) {
+  const float2 dd = dup2(dt), u2 = dup2(uu), yy = dup2(dy);
+  float2 sdus = make_float2(0.f, 0.f), sddt = sdus, sys = sdus;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
+    const float2 Cp = h == 0 ? lo2(C4) : hi2(C4);
+    const float2 snp = h == 0 ? lo2(sn) : hi2(sn);
+    const float2 spp = h == 0 ? lo2(sp) : hi2(sp);  // A h_{t-1}
+    const float2 lam = __ffma2_rn(yy, Cp, carry[h]);
+    const float2 ht = __fmul2_rn(snp, Ik[h]);
+    const float2 dc = __fmul2_rn(yy, ht);
+    sys = __ffma2_rn(Cp, ht, sys);
+    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    const float2 Bu = __fmul2_rn(Bp, u2);
+    const float2 al = __fmul2_rn(ab, lam);
+    float2 r, m;
+    if (DISC == 0) {
+      const float2 q = __fmul2_rn(__fadd2_rn(ab, make_float2(-1.f, -1.f)), Ik[h]);  // (abar - 1) / A
+      r = __fmul2_rn(lam, q);
+      m = __fmul2_rn(al, __fadd2_rn(spp, Bu));                  // abar lambda (A h_{t-1} + B u)
+      dApos[h] = __ffma2_rn(dd, m, dApos[h]);                   // + dt abar lambda v
+      dAneg[h] = __ffma2_rn(r, Bu, dAneg[h]);                   // - q lambda B u
+    } else {
+      r = __fmul2_rn(lam, dd);
+      m = __ffma2_rn(al, spp, __fmul2_rn(lam, Bu));             // lambda (abar A h_{t-1} + B u)
+      dApos[h] = __ffma2_rn(__fmul2_rn(dd, al), spp, dApos[h]); // + dt abar lambda A h_{t-1}
+    }
+    const float2 db = __fmul2_rn(r, u2);
+    sdus = __ffma2_rn(r, Bp, sdus);
+    sddt = __fadd2_rn(sddt, m);
+    carry[h] = al;
+    v[2 * h] = db.x;
+    v[2 * h + 1] = db.y;
+    v[4 + 2 * h] = dc.x;
+    v[4 + 2 * h + 1] = dc.y;
+  }
+  dus = sdus.x + sdus.y;
+  ddt = sddt.x + sddt.y;
+  ys = sys.x + sys.y;
+}
+
+template <int DISC>
+__device__ __forceinline__ void adj_step_precise(float4 sn4, float4 sp4, float4 B4, float4 C4, float dt, float uu,
+                                                 float dy, float (&carry)[4], float (&dAl)[4], const float (&A)[4],
+                                                 const float (&Ik)[4], float (&v)[8], float& dus, float& ddt,
+                                                 float& ys) {
+  const float sn[4] = {sn4.x, sn4.y, sn4.z, sn4.w}, sp[4] = {sp4.x, sp4.y, sp4.z, sp4.w};
+  const float Bv[4] = {B4.x, B4.y, B4.z, B4.w}, Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+  dus = ddt = ys = 0.0f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lam = fmaf(dy, Cv[k], carry[k]);
+    const float Ahp = A[k] * sp[k];
+    v[4 + k] = dy * sn[k];
+    ys = fmaf(Cv[k], sn[k], ys);
+    const float e = expm1f(dt * A[k]);
+    const float ab = 1.0f + e;
+    const float Bu = Bv[k] * uu;
+    const float al = ab * lam;
+    float r, m;
+    if (DISC == 0) {
+      r = lam * (e * Ik[k]);
+      m = al * (Ahp + Bu);
+      dAl[k] = fmaf(dt, m, dAl[k]);
+      dAl[k] = fmaf(-r, Bu, dAl[k]);
+    } else {
+      r = lam * dt;
+      m = fmaf(al, Ahp, lam * Bu);
+      dAl[k] = fmaf(dt * al, Ahp, dAl[k]);
+    }
+    ddt += m;
+    v[k] = r * uu;
+    dus = fmaf(r, Bv[k], dus);
+    carry[k] = al;
+  }
+}
+
+// MODE kBwdFull: the gradients over one time segment (blockIdx.z). MODE
+// kBwdFwdAgg: the end state of segment blockIdx.z from h = 0, and its sum of
+// dt. MODE kBwdAdjAgg: the adjoint carry leaving segment blockIdx.z + 1 at its
+// start when zero enters at its end (and the last segment's sum of dt).
+template <typename Tin, int N, int DISC, bool ALIGNED, int MODE>
+__global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs a) {
+  using G = BwdGeom<Tin, N, ALIGNED>;
+  using E = Elem<Tin>;
+  constexpr bool PRECISE = std::is_same<Tin, float>::value;
+  constexpr int K = G::K, CB = G::CB, LPC = G::LPC, NPL = G::NPL, ES = G::ES;
+  using XCopy2 = TileCopy<ES, G::SBX, CB, K, 2>;  // u, delta
+  using XCopy4 = TileCopy<ES, G::SBX, CB, K, 4>;  // u, delta, z, dout
+  using OCopy3 = TileCopy<ES, G::SBX, CB, K, 3>;  // du, ddelta, dz
+  using BCopy1 = TileCopy<ES, G::SBB, N, K, 1>;   // B
+  using BCopy2 = TileCopy<ES, G::SBB, N, K, 2>;   // B, C
+
+  extern __shared__ __align__(16) unsigned char sm[];
+  const Tin* xs = reinterpret_cast<const Tin*>(sm + G::oX);
+  const Tin* bs = reinterpret_cast<const Tin*>(sm + G::oBC);
+  Tin* os = reinterpret_cast<Tin*>(sm + G::oO);
+  float4* f_tc = reinterpret_cast<float4*>(sm + G::oTC);
+  float* f_dz = reinterpret_cast<float*>(sm + G::oDz);
+  float* red = reinterpret_cast<float*>(sm + G::oRed);
+  float* f_B = reinterpret_cast<float*>(sm + G::oBf);
+  float* f_C = f_B + K * N;
+  float* acc = reinterpret_cast<float*>(sm + G::oAcc);
+  float* ch_bias = reinterpret_cast<float*>(sm + G::oCh);
+  float* ch_D = ch_bias + CB;
+  float4* hist = reinterpret_cast<float4*>(sm + G::oHist);
+
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int c = tid / LPC, part = tid % LPC, n0 = part * NPL;
+  const int b = blockIdx.y;
+  const int Dm = a.dim, L = a.seqlen, nck = a.nchunk, S = a.nseg;
+  const int seg = MODE == kBwdAdjAgg ? int(blockIdx.z) + 1 : int(blockIdx.z);
+  const int seg_t1 = min(L, (seg + 1) * a.seg_len);  // segment = steps [seg * seg_len, seg_t1)
+  const int ci_begin = seg * a.seg_len / K, ci_end = (seg_t1 + K - 1) / K;  // its chunks
+  const int d0 = blockIdx.x * CB;
+  const int nch = min(CB, Dm - d0);
+  const int d = d0 + c;
+  const bool cv = c < nch;
+  const bool has_z = a.z != nullptr;
+  const size_t rowb = (size_t)b * L;
+  // checkpoint slot of chunk ci: ck[((b * nck + ci) * D + d) * N + n0]
+  float* ckp = a.ck + ((size_t)b * nck * Dm + (cv ? d : 0)) * N + n0;
+  const size_t ck_stride = (size_t)Dm * N;
+  const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  if (tid < CB) {
+    const bool ok = tid < nch;
+    ch_bias[tid] = (ok && a.delta_bias) ? a.delta_bias[d0 + tid] : 0.0f;
+    ch_D[tid] = (ok && a.D) ? a.D[d0 + tid] : 0.0f;
+  }
+
+  // A = -exp(A_log), 1/A and (fast path) A log2(e) for my states.
+  float A[NPL], Ik[NPL];
+  float2 A2[2], Al2[2], Ik2[2];
+#pragma unroll
+  for (int k = 0; k < NPL; ++k) {
+    const float al = cv ? a.A_log[(size_t)d * N + n0 + k] : 0.0f;
+    if constexpr (PRECISE) {
+      A[k] = -expf(al);
+      Ik[k] = 1.0f / A[k];
+    } else {
+      A[k] = -hw_ex2(al * kLog2e);
+      Ik[k] = hw_rcp(A[k]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    A2[h] = make_float2(A[2 * h], A[2 * h + 1]);
+    Al2[h] = make_float2(A[2 * h] * kLog2e, A[2 * h + 1] * kLog2e);
+    Ik2[h] = make_float2(Ik[2 * h], Ik[2 * h + 1]);
+  }
+
+  // state: h (fp32 inputs) or s = A h as two pairs (bf16 inputs)
+  float hs[NPL];
+  float2 s2[2];
+  auto load_state = [&](float4 h) {
+    if constexpr (PRECISE) {
+      hs[0] = h.x; hs[1] = h.y; hs[2] = h.z; hs[3] = h.w;
+    } else {
+      s2[0] = __fmul2_rn(lo2(h), A2[0]);
+      s2[1] = __fmul2_rn(hi2(h), A2[1]);
+    }
+  };
+  auto state4 = [&]() -> float4 {  // the state as stored in the history (h or s)
+    if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
+    else return make_float4(s2[0].x, s2[0].y, s2[1].x, s2[1].y);
+  };
+  auto state_h4 = [&]() -> float4 {  // h itself
+    if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
+    else return make_float4(s2[0].x * Ik[0], s2[0].y * Ik[1], s2[1].x * Ik[2], s2[1].y * Ik[3]);
+  };
+  auto fwd_step = [&](float4 B4, float dt, float uu) {
+    if constexpr (PRECISE) fwd_step_precise<DISC>(hs, B4, dt, uu, A, Ik);
+    else fwd_step_fast<DISC>(s2, B4, dt, uu, Al2, A2);
+  };
+
+  // Exponential decay of my states over a segment with the given sum of dt.
+  auto decay = [&](int k, float dsum) { return PRECISE ? expf(A[k] * dsum) : hw_ex2(A[k] * kLog2e * dsum); };
+  auto seg_row = [&](int j) { return ((size_t)b * S + j) * Dm + d; };  // (b, segment j, channel d)
+
+  // ------------------------------------------------ phase 1: checkpoints
+  if constexpr (MODE != kBwdAdjAgg) {
+    float4 h = (MODE == kBwdFull && cv && a.h0) ? ld4(a.h0 + ((size_t)b * Dm + d) * N + n0) : zero4;
+    if constexpr (MODE == kBwdFull) {
+      // the state entering my segment: the segments before it composed onto h0
+      for (int j = 0; j < seg && cv; ++j) {
+        const float ds = a.seg_dsum[seg_row(j)];
+        const float4 e = ld4(a.seg_h + seg_row(j) * N + n0);
+        h = make_float4(fmaf(decay(0, ds), h.x, e.x), fmaf(decay(1, ds), h.y, e.y), fmaf(decay(2, ds), h.z, e.z),
+                        fmaf(decay(3, ds), h.w, e.w));
+      }
+    }
+    load_state(h);
+    float dsum = 0.0f;     // kBwdFwdAgg: sum of dt over the segment (bf16 inputs)
+    double dsum_d = 0.0;   // the same for fp32 inputs
+    XCopy2 xp;
+    BCopy1 bp;
+    auto src_x = [&](int tile) -> const void* { return tile == 0 ? a.u : a.delta; };
+    auto src_b = [&](int) -> const void* { return a.B; };
+    // The full pass stops before its last chunk (its end state is not needed).
+    const int ci_last = MODE == kBwdFull ? ci_end - 1 : ci_end;
+    auto rows_of = [&](int ci) { return min(K, seg_t1 - ci * K); };
+    if (ci_begin < ci_last) {
+      xp.load(src_x, rowb + ci_begin * K, Dm, d0, nch, rows_of(ci_begin), tid);
+      bp.load(src_b, rowb + ci_begin * K, N, 0, N, rows_of(ci_begin), tid);
+    }
+    for (int ci = ci_begin; ci < ci_end; ++ci) {
+      if (MODE == kBwdFull && cv) st4(ckp + ci * ck_stride, state_h4());
+      if (ci == ci_last) break;
+      const int tv = rows_of(ci);
+      __syncthreads();
+      xp.to_smem(sm + G::oX, tid);
+      bp.to_smem(sm + G::oBC, tid);
+      __syncthreads();
+      if (ci + 1 < ci_last) {
+        xp.load(src_x, rowb + (ci + 1) * K, Dm, d0, nch, rows_of(ci + 1), tid);
+        bp.load(src_b, rowb + (ci + 1) * K, N, 0, N, rows_of(ci + 1), tid);
+      }
+      for (int p = tid; p < K * CB; p += kBwdThreads) {
+        const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
+        const bool live = p / CB < tv;  // rows past the segment are exact no-ops
+        f_tc[p] = make_float4(live ? (PRECISE ? softplus_precise(x) : softplus_fast(x)) : 0.0f,
+                              live ? E::load(xs + p) : 0.0f, 0.f, 0.f);
+      }
+      for (int p = tid; p < K * N; p += kBwdThreads) f_B[p] = E::load(bs + p);
+      __syncthreads();
+#pragma unroll 4
+      for (int t = 0; t < K; ++t) {
+        const float4 tc = f_tc[t * CB + c];
+        fwd_step(ld4(f_B + t * N + n0), tc.x, tc.y);
+        if constexpr (MODE == kBwdFwdAgg) {
+          if (PRECISE) dsum_d += tc.x; else dsum += tc.x;
+        }
+      }
+    }
+    if constexpr (MODE == kBwdFwdAgg) {
+      if (cv) {
+        st4(a.seg_h + seg_row(seg) * N + n0, state_h4());
+        if (part == 0) a.seg_dsum[seg_row(seg)] = PRECISE ? float(dsum_d) : dsum;
+      }
+      return;
+    }
+  }
+
+  // --------------------------------------------------- phase 2: adjoint
+  float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs
+  float2 carry2[2], dApos[2], dAneg[2];               // bf16 inputs
+  {
+    float4 g = (MODE == kBwdFull && cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
+    if constexpr (MODE == kBwdFull) {
+      // the adjoint entering my segment from the right: the later segments' carries composed onto dlast
+      for (int j = S - 1; j > seg && cv; --j) {
+        const float ds = a.seg_dsum[seg_row(j)];
+        const float4 e = ld4(a.seg_g + seg_row(j) * N + n0);
+        g = make_float4(fmaf(decay(0, ds), g.x, e.x), fmaf(decay(1, ds), g.y, e.y), fmaf(decay(2, ds), g.z, e.z),
+                        fmaf(decay(3, ds), g.w, e.w));
+      }
+    }
+    carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
+    carry2[0] = lo2(g);
+    carry2[1] = hi2(g);  // (kBwdAdjAgg runs on the scalar carry for either input type)
+    dApos[0] = dApos[1] = dAneg[0] = dAneg[1] = make_float2(0.f, 0.f);
+  }
+  float dD_acc = 0.0f, dbias_acc = 0.0f;  // channel d0 + tid % CB
+  XCopy4 xq;
+  BCopy2 bq;
+  auto src_x4 = [&](int tile) -> const void* {
+    return tile == 0 ? a.u : (tile == 1 ? a.delta : (tile == 2 ? a.z : a.dout));
+  };
+  auto src_bc = [&](int tile) -> const void* { return tile == 0 ? a.B : a.C; };
+  auto dst_o = [&](int tile) -> void* { return tile == 0 ? a.du : (tile == 1 ? a.ddelta : a.dz); };
+  float4 ckn = zero4;
+  float dsum_last = 0.0f;  // kBwdAdjAgg on the last segment: its sum of dt
+  {
+    const int t0 = (ci_end - 1) * K;
+    xq.load(src_x4, rowb + t0, Dm, d0, nch, seg_t1 - t0, tid);
+    bq.load(src_bc, rowb + t0, N, 0, N, seg_t1 - t0, tid);
+    if (MODE == kBwdFull && cv) ckn = ld4(ckp + (ci_end - 1) * ck_stride);
+  }
+  for (int ci = ci_end - 1; ci >= ci_begin; --ci) {
+    const int t0 = ci * K, tv = min(K, seg_t1 - t0);
+    __syncthreads();
+    xq.to_smem(sm + G::oX, tid);
+    bq.to_smem(sm + G::oBC, tid);
+    const float4 cks = ckn;
+    __syncthreads();
+    if (ci > ci_begin) {
+      xq.load(src_x4, rowb + t0 - K, Dm, d0, nch, K, tid);
+      bq.load(src_bc, rowb + t0 - K, N, 0, N, K, tid);
+      if (MODE == kBwdFull && cv) ckn = ld4(ckp + (ci - 1) * ck_stride);
+    }
+    for (int p = tid; p < K * CB; p += kBwdThreads) {
+      const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
+      const float g = E::load(xs + 3 * K * CB + p);
+      const float dt = PRECISE ? softplus_precise(x) : softplus_fast(x);
+      const float sg = PRECISE ? sigmoid_precise(x) : sigmoid_fast(x);
+      float dy = g;
+      if (has_z) {
+        const float zz = E::load(xs + 2 * K * CB + p);
+        const float sz = PRECISE ? sigmoid_precise(zz) : sigmoid_fast(zz);
+        dy = g * zz * sz;                              // dloss/dy = dout SiLU(z)
+        f_dz[p] = g * sz * fmaf(zz, 1.0f - sz, 1.0f);  // dloss/dz = y * this
+      }
+      f_tc[p] = make_float4(dt, E::load(xs + p), dy, sg);
+    }
+    for (int p = tid; p < K * N; p += kBwdThreads) {
+      f_B[p] = E::load(bs + p);
+      f_C[p] = E::load(bs + K * N + p);
+    }
+    __syncthreads();
+
+    if constexpr (MODE == kBwdAdjAgg) {
+      // only the adjoint: lambda_t = dy_t C_t + carry, carry <- abar_t lambda_t
+      for (int t = tv - 1; t >= 0; --t) {
+        const float4 tc = f_tc[t * CB + c];
+        const float4 C4 = ld4(f_C + t * N + n0);
+        const float Cv[4] = {C4.x, C4.y, C4.z, C4.w};
+#pragma unroll
+        for (int k = 0; k < NPL; ++k) {
+          const float ab = PRECISE ? expf(tc.x * A[k]) : hw_ex2(tc.x * A[k] * kLog2e);
+          carry[k] = ab * fmaf(tc.z, Cv[k], carry[k]);
+        }
+        dsum_last += tc.x;
+      }
+      continue;
+    }
+    // recompute the chunk's states: hist[t + 1] = state after step t0 + t
+    // (The operands of the next step are loaded one step ahead: the stores
+    // and shared atomics of a step would otherwise hold back the next step's
+    // loads, which the compiler cannot prove independent.)
+    load_state(cks);
+    hist[tid] = state4();
+    {
+      float4 tc = f_tc[c], B4 = ld4(f_B + n0);
+#pragma unroll 2
+      for (int t = 0; t < tv; ++t) {
+        const int tn = t + 1 < tv ? t + 1 : t;
+        const float4 tc_n = f_tc[tn * CB + c], B4_n = ld4(f_B + tn * N + n0);
+        fwd_step(B4, tc.x, tc.y);
+        hist[(t + 1) * kBwdThreads + tid] = state4();
+        tc = tc_n;
+        B4 = B4_n;
+      }
+    }
+
+    // adjoint, backwards through the chunk, G::SBT steps per round of reductions
+    constexpr int SBT = G::SBT, VPL = G::VPL;
+    float4 sn = state4();  // state after the chunk's last valid step
+    for (int tb = tv - 1; tb >= 0; tb -= SBT) {
+      float vv[SBT * 8];  // per step: dB partials (states n0..n0+3), then dC partials
+      float ww[4 * SBT];  // [quantity][step]: du, dt and y sums over my states, 0
+#pragma unroll
+      for (int si = 0; si < SBT; ++si) {
+        const int t = tb - si;
+        float v[8], dus = 0.0f, ddt = 0.0f, ys = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        if (t >= 0) {  // uniform across the CTA
+          const float4 tc = f_tc[t * CB + c];
+          const float4 sp = hist[t * kBwdThreads + tid];
+          const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
+          if constexpr (PRECISE)
+            adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
+          else
+            adj_step_fast<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, Al2, Ik2, v, dus, ddt, ys);
+          sn = sp;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vv[si * 8 + i] = v[i];
+        ww[si] = dus;
+        ww[SBT + si] = ddt;
+        ww[2 * SBT + si] = ys;
+        ww[3 * SBT + si] = 0.0f;
+      }
+      // (du, dt, y) sums over the channel's LPC lanes: lane part & 3 keeps quantity part & 3
+      reduce_scatter<4 * SBT>(ww, lane, 2);
+      reduce_scatter<2 * SBT>(ww, lane, 1);
+#pragma unroll
+      for (int o = 4; o < LPC; o <<= 1)
+#pragma unroll
+        for (int si = 0; si < SBT; ++si) ww[si] += __shfl_xor_sync(0xffffffffu, ww[si], o);
+      if (part < 3) {
+#pragma unroll
+        for (int si = 0; si < SBT; ++si)
+          if (tb - si >= 0) red[part * K * CB + (tb - si) * CB + c] = ww[si];
+      }
+      // dB, dC summed over the channels of this warp (lane bits >= LPC), highest bit first
+      int jh = 0;
+      if constexpr (G::R >= 1) { reduce_scatter<8 * SBT>(vv, lane, 16); jh = (lane >> 4) & 1; }
+      if constexpr (G::R >= 2) { reduce_scatter<4 * SBT>(vv, lane, 8); jh = jh * 2 + ((lane >> 3) & 1); }
+      if constexpr (G::R >= 3) { reduce_scatter<2 * SBT>(vv, lane, 4); jh = jh * 2 + ((lane >> 2) & 1); }
+#pragma unroll
+      for (int g = 0; g < VPL / 4; ++g) {
+        const int j0 = jh * VPL + 4 * g;  // index of (step, dB|dC, state n0) in vv
+        const int t = tb - (j0 >> 3);
+        if (t >= 0)
+          st4(acc + ((tid >> 5) * K + t) * 2 * N + ((j0 >> 2) & 1) * N + n0,
+              make_float4(vv[4 * g], vv[4 * g + 1], vv[4 * g + 2], vv[4 * g + 3]));
+      }
+    }
+    __syncthreads();
+    // per (t, channel): du = sum + dy D, ddelta = dt-sum * sigmoid, dz = (y-sum + D u) * factor
+    for (int p = tid; p < tv * CB; p += kBwdThreads) {
+      const int cc = p % CB;  // == tid % CB
+      const float4 tc = f_tc[p];
+      const float Dd = ch_D[cc];
+      const float dd = red[K * CB + p] * tc.w;
+      E::store(os + p, fmaf(tc.z, Dd, red[p]));
+      E::store(os + K * CB + p, dd);
+      if (has_z) E::store(os + 2 * K * CB + p, fmaf(Dd, tc.y, red[2 * K * CB + p]) * f_dz[p]);
+      dD_acc = fmaf(tc.z, tc.y, dD_acc);
+      dbias_acc += dd;
+    }
+    for (int i = tid * 4; i < tv * 2 * N; i += kBwdThreads * 4) {
+      const int t = i / (2 * N), j = i - t * 2 * N;
+      float4 sum = ld4(acc + i);
+#pragma unroll
+      for (int w = 1; w < G::NW; ++w) {
+        const float4 x = ld4(acc + w * K * 2 * N + i);
+        sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+      }
+      float* dst = (j < N ? a.dB : a.dC) + (rowb + t0 + t) * N + (j < N ? j : j - N);
+      atomicAdd(reinterpret_cast<float4*>(dst), sum);
+    }
+    __syncthreads();
+    OCopy3::smem_to_global(sm + G::oO, dst_o, rowb + t0, Dm, d0, nch, tv, tid);
+  }
+
+  if constexpr (MODE == kBwdAdjAgg) {
+    if (cv) {
+      st4(a.seg_g + seg_row(seg) * N + n0, make_float4(carry[0], carry[1], carry[2], carry[3]));
+      if (part == 0 && seg == S - 1) a.seg_dsum[seg_row(seg)] = dsum_last;
+    }
+    return;
+  }
+  if (cv) {
+    float4 dA4, g4;
+    if constexpr (PRECISE) {
+      dA4 = make_float4(dAl[0], dAl[1], dAl[2], dAl[3]);
+      g4 = make_float4(carry[0], carry[1], carry[2], carry[3]);
+    } else {
+      dA4 = make_float4(dApos[0].x - dAneg[0].x, dApos[0].y - dAneg[0].y, dApos[1].x - dAneg[1].x,
+                        dApos[1].y - dAneg[1].y);
+      g4 = make_float4(carry2[0].x, carry2[0].y, carry2[1].x, carry2[1].y);
+    }
+    atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), dA4);
+    if (a.dh0 && seg == 0) st4(a.dh0 + ((size_t)b * Dm + d) * N + n0, g4);
+  }
+  if ((tid % CB) < nch) {
+    if (a.dD) atomicAdd(a.dD + d0 + tid % CB, dD_acc);
+    if (a.ddelta_bias) atomicAdd(a.ddelta_bias + d0 + tid % CB, dbias_acc);
+  }
+}
+
+template <typename Tin, int N, int DISC, bool ALIGNED, int MODE>
+cudaError_t launch_bwd_variant(const BwdArgs& a, unsigned nz, cudaStream_t stream) {
+  using G = BwdGeom<Tin, N, ALIGNED>;
+  static bool configured = false;  // per instantiation; benign race (idempotent)
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<Tin, N, DISC, ALIGNED, MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const dim3 grid((a.dim + G::CB - 1) / G::CB, a.batch, nz);
+  scan_bwd_kernel<Tin, N, DISC, ALIGNED, MODE><<<grid, kBwdThreads, G::kSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename Tin, int N, int MODE>
+cudaError_t launch_bwd_n(const BwdArgs& a, unsigned nz, cudaStream_t stream) {
+  if (a.disc == 0)
+    return a.aligned ? launch_bwd_variant<Tin, N, 0, true, MODE>(a, nz, stream)
+                     : launch_bwd_variant<Tin, N, 0, false, MODE>(a, nz, stream);
+  return a.aligned ? launch_bwd_variant<Tin, N, 1, true, MODE>(a, nz, stream)
+                   : launch_bwd_variant<Tin, N, 1, false, MODE>(a, nz, stream);
+}
+
+template <typename Tin, int MODE>
+cudaError_t launch_bwd_typed(const BwdArgs& a, unsigned nz, cudaStream_t stream) {
+  switch (a.dstate) {
+    case 16: return launch_bwd_n<Tin, 16, MODE>(a, nz, stream);
+    case 32: return launch_bwd_n<Tin, 32, MODE>(a, nz, stream);
+    case 64: return launch_bwd_n<Tin, 64, MODE>(a, nz, stream);
+    case 128: return launch_bwd_n<Tin, 128, MODE>(a, nz, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_bwd_mode(int dtype, const BwdArgs& a, unsigned nz, cudaStream_t stream) {
+  return dtype == 0 ? launch_bwd_typed<float, MODE>(a, nz, stream)
+                    : launch_bwd_typed<__nv_bfloat16, MODE>(a, nz, stream);
+}
+
+}  // namespace
+}  // namespace mamba

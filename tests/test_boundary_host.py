@@ -166,3 +166,8 @@ def test_bwd_rejects_bad_arguments(lib, kw, status):
 def test_bwd_empty_problem_is_ok_without_a_device(lib):
     # nothing to zero and nothing to launch
     assert lib.mamba_selective_scan_bwd(*_bwd_args(batch=0, dim=0)) == 0
+
+
+def test_bwd_ex_rejects_negative_segments(lib):
+    args = _bwd_args()
+    assert lib.mamba_selective_scan_bwd_ex(*args[:-1], -1, None) == 1

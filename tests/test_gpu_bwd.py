@@ -27,7 +27,8 @@ def dev():
     return torch.device("cuda:0")
 
 
-def run_gpu_bwd(inp, dev, disc=0, with_z=True, with_D=True, with_bias=True, with_h0=False, with_dlast=False):
+def run_gpu_bwd(inp, dev, disc=0, with_z=True, with_D=True, with_bias=True, with_h0=False, with_dlast=False,
+                segments=None):
     import torch
     from selective_state_space_125_b300 import binding
     dt = inp["dtype"]
@@ -39,7 +40,7 @@ def run_gpu_bwd(inp, dev, disc=0, with_z=True, with_D=True, with_bias=True, with
         delta_bias=f32(inp["delta_bias"]) if with_bias else None,
         initial_state=f32(inp["h0"]) if with_h0 else None,
         dlast_state=f32(inp["dlast"]) if with_dlast else None,
-        discretization=disc, need_dD=True, need_ddelta_bias=True, need_dinitial_state=True)
+        discretization=disc, need_dD=True, need_ddelta_bias=True, need_dinitial_state=True, segments=segments)
     torch.cuda.synchronize()
     assert binding.mamba_device_status() == 0
     out = {k: (None if v is None else to_numpy(v)) for k, v in g.items()}
@@ -73,11 +74,12 @@ def assert_grads(got, ref, dtype, what):
     return errs
 
 
-def check(batch, dim, dstate, seqlen, dtype, seed=0, disc=0, **opts):
-    inp = make_bwd_inputs(batch, dim, dstate, seqlen, dtype, seed)
-    got = run_gpu_bwd(inp, dev_holder["dev"], disc, **opts)
+def check(batch, dim, dstate, seqlen, dtype, seed=0, disc=0, segments=None, dt_range=(1e-3, 1e-1), **opts):
+    inp = make_bwd_inputs(batch, dim, dstate, seqlen, dtype, seed, dt_range=dt_range)
+    got = run_gpu_bwd(inp, dev_holder["dev"], disc, segments=segments, **opts)
     ref = run_oracle_bwd(inp, disc, **opts)
-    return assert_grads(got, ref, dtype, f"B{batch} D{dim} N{dstate} L{seqlen} {dtype} disc{disc} {opts}")
+    return assert_grads(got, ref, dtype,
+                        f"B{batch} D{dim} N{dstate} L{seqlen} {dtype} disc{disc} segments={segments} {opts}")
 
 
 dev_holder = {}
@@ -213,3 +215,37 @@ def test_bwd_under_cuda_graph_capture():
         assert torch.equal(eager[k], captured[k]), k
     for k in ("dA_log", "dB", "dC", "dD", "ddelta_bias"):
         assert parity_err(to_numpy(captured[k]), to_numpy(eager[k])) < 1e-5, k
+
+
+# ---- time segments: the forward and adjoint segment passes composed by the gradient pass
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("segments", [2, 3, 7])
+@pytest.mark.parametrize("shape", [(2, 64, 16, 300), (1, 40, 16, 333)])
+def test_bwd_segments(dtype, segments, shape):
+    check(*shape, dtype, seed=10 + segments, segments=segments, with_h0=True, with_dlast=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_segments_simplified_and_n64(dtype):
+    check(2, 48, 64, 170, dtype, seed=20, disc=1, segments=3, with_h0=True, with_dlast=True)
+    check(1, 48, 64, 170, dtype, seed=21, disc=0, segments=4, with_h0=True, with_dlast=True)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_bwd_segments_optional_inputs_absent(dtype):
+    check(2, 64, 16, 260, dtype, seed=22, segments=3, with_z=False, with_D=False, with_bias=False)
+
+
+def test_bwd_automatic_segments_on_a_long_narrow_sequence():
+    # 1 x 64 channels: 2 CTAs, so the planner cuts the 2048 steps into segments; wide dt range
+    check(1, 64, 16, 2048, "f32", seed=23, segments=0, dt_range=(1e-4, 1.0), with_h0=True, with_dlast=True)
+    check(1, 64, 16, 2048, "bf16", seed=24, segments=0, with_h0=True, with_dlast=True)
+
+
+def test_bwd_segments_agree_with_one_segment():
+    inp = make_bwd_inputs(2, 64, 16, 400, "f32", 25)
+    dev = dev_holder["dev"]
+    one = run_gpu_bwd(inp, dev, segments=1, with_h0=True, with_dlast=True)
+    five = run_gpu_bwd(inp, dev, segments=5, with_h0=True, with_dlast=True)
+    for k in GRADS:
+        assert parity_err(five[k], one[k]) < 1e-5, k
