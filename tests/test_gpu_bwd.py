@@ -249,3 +249,54 @@ def test_bwd_segments_agree_with_one_segment():
     five = run_gpu_bwd(inp, dev, segments=5, with_h0=True, with_dlast=True)
     for k in GRADS:
         assert parity_err(five[k], one[k]) < 1e-5, k
+
+
+# ---- full-size workloads, in the launch configuration bench.py times, on sampled outputs
+def _bwd_full_size(B, D, L, dt_range, seed, chans, dbdc_row):
+    import torch
+    from selective_state_space_125_b300 import binding
+    dev = dev_holder["dev"]
+    inp = make_bwd_inputs(B, D, 16, L, "bf16", seed, dt_range=dt_range)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    t = {k: to_torch(inp[k], "bf16", dev) for k in ("u", "delta", "z", "B", "C", "dout")}
+    g = binding.mamba_selective_scan_bwd(t["u"], t["delta"], f32(inp["A_log"]), t["B"], t["C"], t["dout"],
+                                         D=f32(inp["D"]), z=t["z"], delta_bias=f32(inp["delta_bias"]),
+                                         initial_state=f32(inp["h0"]), dlast_state=f32(inp["dlast"]))
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    got = {k: to_numpy(v) for k, v in g.items() if v is not None}
+    del t, g
+    # per-channel gradients: the oracle on the sampled channels, every batch row and step
+    sl = lambda a: np.ascontiguousarray(a[:, :, chans])
+    ref = oracle.selective_scan_bwd(sl(inp["u"]), sl(inp["delta"]), inp["A_log"][chans], inp["B"], inp["C"],
+                                    sl(inp["dout"]), D=inp["D"][chans], z=sl(inp["z"]),
+                                    delta_bias=inp["delta_bias"][chans], h0=inp["h0"][:, chans],
+                                    dlast=inp["dlast"][:, chans])
+    errs = {"du": parity_err(got["du"][:, :, chans], ref["du"]),
+            "ddelta": parity_err(got["ddelta"][:, :, chans], ref["ddelta"]),
+            "dz": parity_err(got["dz"][:, :, chans], ref["dz"]),
+            "dA_log": parity_err(got["dA_log"][chans], ref["dA_log"]),
+            "dD": parity_err(got["dD"][chans], ref["dD"]),
+            "ddelta_bias": parity_err(got["ddelta_bias"][chans], ref["ddelta_bias"]),
+            "dh0": parity_err(got["dinitial_state"][:, chans], ref["dh0"])}
+    if dbdc_row is not None:
+        # dB, dC sum over every channel: the oracle on one whole batch row
+        r = slice(dbdc_row, dbdc_row + 1)
+        full = oracle.selective_scan_bwd(inp["u"][r], inp["delta"][r], inp["A_log"], inp["B"][r], inp["C"][r],
+                                         inp["dout"][r], D=inp["D"], z=inp["z"][r], delta_bias=inp["delta_bias"],
+                                         h0=inp["h0"][r], dlast=inp["dlast"][r])
+        errs["dB"] = parity_err(got["dB"][r], full["dB"])
+        errs["dC"] = parity_err(got["dC"][r], full["dC"])
+    bad = {k: e for k, e in errs.items() if not e <= TOL["bf16"]}
+    assert not bad, ", ".join(f"{k} {e:.2e}" for k, e in sorted(errs.items()))
+
+
+def test_bwd_full_size_m130_sampled():
+    """B8 D1536 N16 L2048 (the bench's backward workload): 12 sampled channels in full, dB/dC of row 3."""
+    chans = [0, 1, 31, 32, 511, 777, 1000, 1023, 1024, 1500, 1534, 1535]
+    _bwd_full_size(8, 1536, 2048, (1e-3, 1e-1), 0, chans, dbdc_row=3)
+
+
+def test_bwd_full_size_long_sequence_sampled():
+    """B1 D5120 N16 L32768 with automatic time segments: 6 sampled channels over the whole sequence."""
+    _bwd_full_size(1, 5120, 32768, (1e-4, 1.0), 0, [0, 1, 2047, 2048, 5000, 5119], dbdc_row=None)
