@@ -163,11 +163,20 @@ int npl_for(int N, int lpc) {
 //    the same steps, less than the lane-sharing overhead and the idle SMs it
 //    replaces;
 //  - otherwise the states of a channel are spread over up to 4 lanes to
-//    reach 8 warps per SM, then time is split if that is still short.
+//    reach 8 warps per SM;
+//  - then, if fewer than 2 CTAs per SM result, time is split into segments of
+//    at least kMinSegSteps steps, aiming at 8 CTAs per SM (at most 64
+//    segments). Batch-1 prefill shapes on B300 (L 2048: B1 x D 1536 / 2560 /
+//    5120) ran in 60 / 89 / 151 us with 8 segments, against 84 / 103 / 195 us
+//    with the 4 / 4 / 2 segments of a 256-threads-per-SM target and
+//    512-step minimum; B1 D1536 L8192 ran in 200 us with 32 segments against
+//    257 us with 16. Layers with 2 or more CTAs per SM (the 130M- and
+//    1.4B-shaped ones) stay unsplit: a split adds an aggregate pass and a
+//    second wave.
 constexpr int kTargetThreadsPerSM = 256;
-constexpr int kLongTargetThreadsPerSM = 1024;
+constexpr int kSplitTargetCtasPerSM = 8;
 constexpr int kLongSeq = 8192;
-constexpr int kMinSegSteps = 512;
+constexpr int kMinSegSteps = 256;
 
 struct Plan {
   int npl, lpc, nseg, seg_len, chunk;
@@ -206,10 +215,10 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
 
   const int max_seg = std::max(1, std::min(65535, (L + v.chunk - 1) / v.chunk));
   if (nseg == 0) {
-    const long long threads = channels * lpc;
-    const long long want = long_split ? (long long)sms * kLongTargetThreadsPerSM : target;
+    const long long ctas = (channels * lpc + kScanThreads - 1) / kScanThreads;
+    const long long want = (long long)sms * kSplitTargetCtasPerSM;
     nseg = 1;
-    if (threads < want) nseg = int((want + threads - 1) / threads);
+    if (ctas < 2LL * sms) nseg = int((want + ctas - 1) / ctas);
     // segments of at least kMinSegSteps steps, at most 64 segments
     nseg = std::min({nseg, 64, std::max(1, L / kMinSegSteps)});
   }
