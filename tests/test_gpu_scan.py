@@ -301,3 +301,22 @@ def test_segmented_scan_under_cuda_graph_capture(dev):
     torch.cuda.synchronize()
     assert binding.mamba_device_status() == 0
     assert torch.equal(out, eager) and torch.equal(last, eager_last)
+
+
+@pytest.mark.parametrize("shape,want", [
+    ((8, 1536, 2048), (4, 1)),     # the 130M-shaped layer: 2.6 CTAs per SM, no split
+    ((16, 4096, 2048), (1, 1)),    # the 1.4B-shaped layer: one lane per channel, no split
+    ((1, 5120, 32768), (1, 30)),   # the long sequence
+    ((1, 1536, 2048), (4, 8)),     # batch-1 prefill: split towards 8 CTAs per SM
+    ((1, 1536, 8192), (1, 32)),
+])
+def test_planner_choices(dev, shape, want):
+    """The automatic plans the tuning in the planner's comments was measured on (148-SM B300)."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    if torch.cuda.get_device_properties(dev).multi_processor_count != 148:
+        pytest.skip("plans are tuned for 148 SMs")
+    B, D, L = shape
+    chosen, launches = binding.mamba_selective_scan_plan(B, D, 16, L, "bf16")
+    assert (chosen.lanes_per_channel, chosen.segments) == want
+    assert launches == (1 if want[1] == 1 else 2)
