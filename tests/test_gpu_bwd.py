@@ -300,3 +300,11 @@ def test_bwd_full_size_m130_sampled():
 def test_bwd_full_size_long_sequence_sampled():
     """B1 D5120 N16 L32768 with automatic time segments: 6 sampled channels over the whole sequence."""
     _bwd_full_size(1, 5120, 32768, (1e-4, 1.0), 0, [0, 1, 2047, 2048, 5000, 5119], dbdc_row=None)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape,segments", [((2, 36, 16, 90), 3),     # element-by-element loader
+                                            ((1, 48, 32, 130), 4),
+                                            ((1, 20, 128, 100), 2)])  # one warp per channel
+def test_bwd_segments_other_layouts(dtype, shape, segments):
+    check(*shape, dtype, seed=30 + segments, segments=segments, with_h0=True, with_dlast=True)
