@@ -171,3 +171,35 @@ def test_bwd_empty_problem_is_ok_without_a_device(lib):
 def test_bwd_ex_rejects_negative_segments(lib):
     args = _bwd_args()
     assert lib.mamba_selective_scan_bwd_ex(*args[:-1], -1, None) == 1
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include "mamba_ssm.h"
+int main(void) {
+    int v = mamba_version();
+    /* every call below is rejected by validation, before any CUDA call */
+    mamba_status_t s1 = mamba_selective_scan_bwd(1, 8, 8, 4, MAMBA_BF16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0,
+                                                 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    mamba_status_t s2 = mamba_selective_scan_fwd(-1, 8, 16, 4, MAMBA_BF16, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    mamba_status_t s3 = mamba_selective_state_update_ex(1, 8, 16, MAMBA_F32, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 7, 0);
+    printf("%d %d %d %d %s\n", v, (int)s1, (int)s2, (int)s3, mamba_last_error_detail());
+    return 0;
+}
+"""
+
+
+def test_plain_c_client_links_and_calls_the_abi(lib, tmp_path):
+    """The library is a C ABI: a C99 program (no Python, no torch) compiles against the
+    header, links the shared library and gets its statuses."""
+    import subprocess
+    from selective_state_space_125_b300 import binding
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(binding.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-lmamba_ssm_b300", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    assert int(out[0]) == lib.mamba_version()
+    assert out[1:4] == ["2", "1", "1"]  # unsupported N; negative size; unknown discretisation
