@@ -1,6 +1,8 @@
 /*
  * mamba_ssm.h - C ABI of libmamba_ssm_b300.so, the B300 (sm_103a) selective
- * state-space scan of Mamba and its single-token decode step.
+ * state-space scan of Mamba, its single-token decode step, the scan with a
+ * causal conv1d + SiLU fused in front, and the scan's backward (gradients of
+ * every input).
  *
  * The operation (page titles and passages that define it):
  *   "State Space Models and Mamba" (jonathanding.github.io, llm-learning)
@@ -24,7 +26,8 @@
  *     y       = sum_n C[b,t,n] h[n] + D[d] u[b,t,d]
  *     out     = y * z / (1 + exp(-z))        (z = z[b,t,d]; no gate if z is NULL)
  * from h = 0 (or from initial_state in the _ex entry point). The decode step
- * is the same body for one token on a state kept in device memory.
+ * is the same body for one token on a state kept in device memory. The
+ * backward returns the gradients of sum(dout * out) + sum(dlast * last_state).
  *
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers owned by the caller unless said otherwise;
@@ -45,7 +48,7 @@
  *     fp32 with fp32 state. With MAMBA_F32 inputs the kernels use accurate
  *     expm1/exp/log1p; with MAMBA_BF16 inputs they use the hardware ex2/lg2
  *     approximations (relative error of Bbar about 2^-22 / |dt A|).
- *   - dstate (N) may be 1..256.
+ *   - dstate (N) may be 1..256 (16, 32, 64 or 128 for the backward).
  */
 #ifndef MAMBA_SSM_H
 #define MAMBA_SSM_H
