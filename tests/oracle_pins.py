@@ -353,6 +353,61 @@ def pin_simplified_variant_geometric(orc, seed=10):
     return max(errs)
 
 
+
+def pin_decode_simplified_closed_form(orc, seed=14):
+    """The decode step's variant 1 (Bbar = dt B): with N = 1, A = -exp(A_log), B = C = 1,
+    no D and no gate, k steps of constant dt and u from h0 give
+    h_k = a^k h0 + dt u (1 - a^k) / (1 - a), a = exp(dt A), and out = h_k (geometric
+    series of the recurrence, [SSM] §3). Several channels and batch rows, each with its
+    own dt, A and u, are stepped together so that a channel or row mix-up shows."""
+    rng = np.random.default_rng(seed)
+    batch, dim, K = 2, 3, 12
+    A_log = rng.uniform(-1.0, 1.0, (dim, 1))
+    s = rng.uniform(-3.0, 1.0, (batch, dim))          # delta (no bias)
+    u = rng.standard_normal((batch, dim))
+    h0 = rng.standard_normal((batch, dim, 1))
+    A = -np.exp(A_log[:, 0])[None, :]
+    dt = softplus_ref(s)
+    a = np.exp(dt * A)
+    state = h0.copy()
+    errs = []
+    ones = np.ones((batch, 1))
+    for k in range(1, K + 1):
+        state, out = orc.state_update(state, u, s, A_log, ones, ones, variant=1)
+        ref = a ** k * h0[:, :, 0] + dt * u * (1.0 - a ** k) / (1.0 - a)
+        errs.append(rel_err(state[:, :, 0], ref))
+        errs.append(rel_err(out, ref))
+    return max(errs)
+
+
+def pin_tiny_A_integrates(orc, seed=15):
+    """|A| -> 0 (A_log very negative, long memory): exp(dt A) -> 1 and the
+    zero-order-hold input matrix (exp(dt A) - 1) / A B -> dt B ([SSM] §2, the limit
+    of the ODE solution as A -> 0), so the state integrates dt B u without decay:
+    h_t = h0 + sum_{s<=t} dt_s B_s u_s, y_t = C_t h_t + D u_t. Checked for A_log down
+    to -800, where exp(A_log) is 0 in double precision, in the scan and the decode step."""
+    rng = np.random.default_rng(seed)
+    batch, L, dim, N = 2, 30, 2, 4
+    A_log = np.array([[-40.0, -80.0, -200.0, -800.0], [-60.0, -120.0, -400.0, -745.0]])
+    u = rng.standard_normal((batch, L, dim))
+    delta = rng.uniform(-6.0, 2.0, (batch, L, dim))
+    B = rng.standard_normal((batch, L, N))
+    C = rng.standard_normal((batch, L, N))
+    D = rng.standard_normal(dim)
+    h0 = rng.standard_normal((batch, dim, N))
+    dt = softplus_ref(delta)                                     # (b, t, d)
+    inc = dt[:, :, :, None] * B[:, :, None, :] * u[:, :, :, None]  # (b, t, d, n)
+    h = h0[:, None, :, :] + np.cumsum(inc, axis=1)               # (b, t, d, n)
+    y = np.einsum("btdn,btn->btd", h, C) + D * u
+    out, last = orc.selective_scan(u, delta, A_log, B, C, D, h0=h0)
+    errs = [rel_err(out, y), rel_err(last, h[:, -1])]
+    state = h0.copy()
+    for t in range(L):
+        state, o = orc.state_update(state, u[:, t], delta[:, t], A_log, B[:, t], C[:, t], D)
+        errs.append(rel_err(o, y[:, t]))
+    errs.append(rel_err(state, h[:, -1]))
+    return max(errs)
+
 def _conv_ref_numpy(x, w, bias):
     """Causal depthwise convolution by numpy.convolve (full mode, first L
     outputs): an independent restatement of the same definition."""
@@ -600,6 +655,8 @@ PINS = {
     "continuation": (pin_continuation, 1e-12),
     "structure": (pin_structure, 1e-12),
     "simplified_variant_geometric": (pin_simplified_variant_geometric, 1e-12),
+    "decode_simplified_closed_form": (pin_decode_simplified_closed_form, 1e-12),
+    "tiny_A_integrates": (pin_tiny_A_integrates, 1e-12),
     "conv_identity_tap": (pin_conv_identity_tap, 1e-14),
     "conv_matches_numpy": (pin_conv_matches_numpy, 1e-12),
     "conv_causal_window": (pin_conv_causal_window, 0.0),

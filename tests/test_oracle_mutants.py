@@ -37,6 +37,12 @@ MUTANTS = {
     "decode_A_index": ("const double A_n = -exp(A_log[d * dstate + n]);",
                        "const double A_n = -exp(A_log[n]);"),
     "decode_state_not_decayed": ("*h = abar * (*h) + bbar * u[i];", "*h = (*h) + bbar * u[i];"),
+    # the decode step ignores its variant flag (always zero-order hold)
+    "decode_variant_ignored": ("const double bbar = oracle_bbar(dt, A_n, B[b * dstate + n], variant);",
+                               "const double bbar = oracle_bbar(dt, A_n, B[b * dstate + n], 0);"),
+    # the A -> 0 limit of the input matrix taken as 0 instead of dt B
+    "zoh_limit_dropped": ("double phi = (dA == 0.0) ? 1.0 : expm1(dA) / dA;",
+                          "double phi = (dA == 0.0) ? 0.0 : expm1(dA) / dA;"),
     "conv_taps_reversed": ("acc += w[d * width + k] * x[(b * seqlen + ts) * dim + d];",
                            "acc += w[d * width + (width - 1 - k)] * x[(b * seqlen + ts) * dim + d];"),
     "conv_without_silu": ("u[(b * seqlen + t) * dim + d] = oracle_silu(acc);",
