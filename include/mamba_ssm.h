@@ -47,7 +47,16 @@
  *     out. A_log, D, delta_bias, states are always fp32. All arithmetic is
  *     fp32 with fp32 state. With MAMBA_F32 inputs the kernels use accurate
  *     expm1/exp/log1p; with MAMBA_BF16 inputs they use the hardware ex2/lg2
- *     approximations (relative error of Bbar about 2^-22 / |dt A|).
+ *     approximations, and take exp(dt A) - 1 from a short series wherever
+ *     dt |A| is small enough that ex2 - 1 would cancel (the scan and the
+ *     backward switch per chunk or step when some state of the block falls
+ *     below dt |A| = 2^-14 or 2^-12; the decode step always does), so that
+ *     Bbar keeps a relative error near 1e-6 at any dt A.
+ *   - |A| = exp(A_log) is floored at 1e-20 inside the kernels. At and below
+ *     that floor exp(dt A) and (exp(dt A) - 1) / A equal their A -> 0 limits
+ *     (1 and dt) in fp32 for any dt below 1e12, so results are those of the
+ *     exact A (the zero-order hold's limit: the state integrates dt B u).
+ *     The backward multiplies dA_log = A dloss/dA by the unfloored A.
  *   - dstate (N) may be 1..256 (16, 32, 64 or 128 for the backward).
  */
 #ifndef MAMBA_SSM_H
@@ -230,12 +239,11 @@ MAMBA_API mamba_status_t mamba_selective_scan_plan(
  *   D, delta_bias : (D,) fp32 or NULL.
  *   out        : (B, D) in_dtype, written.
  * MAMBA_F32 inputs use expf / expm1f / log1pf. MAMBA_BF16 inputs use the
- * hardware ex2 / rcp approximations. With N a power of two from 8 to 256, dim
- * a multiple of 8 and 16-byte aligned pointers, zero-order hold runs on the
- * scaled state A h, as the bf16 scan does. The input term then has a relative
- * error of about 2^-22 / |dt A| (2e-4 at dt A = 1e-3). Other shapes take
- * exp(dt A) - 1 from a short series where dt A is small (relative error near
- * 1e-6). batch may be up to 262140.
+ * hardware ex2 / rcp approximations, with exp(dt A) - 1 from a short series
+ * where |dt A| < 1/8 (relative error near 1e-6 at any dt A). With N a power of
+ * two from 8 to 256, dim a multiple of 8 and 16-byte aligned pointers, the
+ * state is staged through shared memory by bulk copies (the bulk-staged
+ * kernel); other shapes take a register-path kernel. batch may be up to 262140.
  */
 MAMBA_API mamba_status_t mamba_selective_state_update(
     int batch, int dim, int dstate, mamba_dtype_t in_dtype,
@@ -337,6 +345,18 @@ MAMBA_API mamba_status_t mamba_device_status(int *status_out, mamba_stream_t str
 
 /* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
 MAMBA_API int mamba_version(void);
+
+/*
+ * Test setting, process-wide: the limit, in nanoseconds, that the scan and
+ * decode launches enqueued after this call give their pipeline's mbarrier
+ * waits (default 2000000000, 2 s). 0 makes those waits give up at once, so
+ * that a launch that waits on a copy records MAMBA_ERR_TIMEOUT in the device
+ * status word and returns early without writing all of its outputs; its
+ * copies already in flight are still awaited with the default limit before
+ * it exits. This exists to exercise the timeout path on a healthy GPU; leave
+ * it at the default otherwise. Returns the previous limit.
+ */
+MAMBA_API unsigned long long mamba_set_wait_limit_ns(unsigned long long limit_ns);
 
 #ifdef __cplusplus
 }

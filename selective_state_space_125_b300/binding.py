@@ -29,7 +29,7 @@ EXPORTED = ("mamba_selective_scan_fwd", "mamba_selective_scan_fwd_ex",
             "mamba_last_error_detail", "mamba_device_status", "mamba_version",
             "mamba_selective_scan_plan", "mamba_selective_scan_fwd_noalloc",
             "mamba_selective_state_update_ex", "mamba_conv1d_selective_scan_fwd",
-            "mamba_selective_scan_bwd", "mamba_selective_scan_bwd_ex")
+            "mamba_selective_scan_bwd", "mamba_selective_scan_bwd_ex", "mamba_set_wait_limit_ns")
 
 _lock = threading.Lock()
 _lib = None
@@ -88,6 +88,8 @@ def library() -> ctypes.CDLL:
             lib.mamba_selective_scan_plan.restype = i
             lib.mamba_version.argtypes = []
             lib.mamba_version.restype = i
+            lib.mamba_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+            lib.mamba_set_wait_limit_ns.restype = ctypes.c_ulonglong
             _lib = lib
     return _lib
 
@@ -321,6 +323,12 @@ def mamba_selective_scan_plan(batch, dim, dstate, seqlen, dtype="bf16", plan=Non
                                               ctypes.byref(plan) if plan is not None else None,
                                               ctypes.byref(chosen), ctypes.byref(launches)))
     return chosen, launches.value
+
+
+def mamba_set_wait_limit_ns(limit_ns: int) -> int:
+    """Test setting: the mbarrier wait limit (ns) of later scan and decode
+    launches (0 gives up at once). Returns the previous limit."""
+    return int(library().mamba_set_wait_limit_ns(int(limit_ns)))
 
 
 def mamba_device_status(stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -36,7 +37,8 @@ __device__ int g_mamba_status_word;
 
 namespace {
 
-constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kVersion = 1 * 10000 + 1 * 100 + 0;
+constexpr unsigned long long kWaitLimitNsDefault = 2000000000ull;  // the kernels' default wait limit (2 s)
 constexpr int kMaxState = 256;
 constexpr int kMaxDevices = 64;
 
@@ -146,10 +148,11 @@ cudaError_t launch_scan_pass(int dtype, int disc, int npl, int lpc, ScanMode mod
 }
 
 // States per thread for `lpc` threads per channel: the smallest of 4, 8, 16
-// that covers N; 0 if none does.
-int npl_for(int N, int lpc) {
+// that covers N with a kernel built for it; 0 if none does.
+int npl_for(int dtype, int N, int lpc) {
+  ScanVariant v;
   for (int npl : {4, 8, 16})
-    if (npl * lpc >= N) return npl;
+    if (npl * lpc >= N && variant_for(dtype, npl, lpc, &v)) return npl;
   return 0;
 }
 
@@ -179,7 +182,7 @@ constexpr int kLongSeq = 8192;
 constexpr int kMinSegSteps = 256;
 
 struct Plan {
-  int npl, lpc, nseg, seg_len, chunk;
+  int npl, lpc, cb, nseg, seg_len, chunk;
   bool tma_x, tma_bc;
 };
 
@@ -199,23 +202,22 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
     if (!long_split) {
       // Spread a channel's states over more threads while that is needed to
       // fill the device, up to 4 lanes and at least 4 real states per lane.
-      ScanVariant probe;
       while (channels * lpc < target && lpc * 2 <= std::max(4, lpc_min) && N >= 4 * lpc * 2 &&
-             variant_for(dtype, npl_for(N, lpc * 2), lpc * 2, &probe))
+             npl_for(dtype, N, lpc * 2) != 0)
         lpc *= 2;
     }
   }
   if (lpc < lpc_min || (lpc & (lpc - 1)) != 0 || lpc > 16)
     return fail(MAMBA_ERR_INVALID_ARG, "lanes_per_channel=%d is not a power of two in [%d, 16] for N=%d", lpc,
                 lpc_min, N);
-  const int npl = npl_for(N, lpc);
+  const int npl = npl_for(dtype, N, lpc);
   ScanVariant v;
   if (npl == 0 || !variant_for(dtype, npl, lpc, &v))
     return fail(MAMBA_ERR_UNSUPPORTED, "no scan kernel for N=%d with lanes_per_channel=%d", N, lpc);
 
   const int max_seg = std::max(1, std::min(65535, (L + v.chunk - 1) / v.chunk));
   if (nseg == 0) {
-    const long long ctas = (channels * lpc + kScanThreads - 1) / kScanThreads;
+    const long long ctas = ((long long)dim + v.cb - 1) / v.cb * batch;
     const long long want = (long long)sms * kSplitTargetCtasPerSM;
     nseg = 1;
     if (ctas < 2LL * sms) nseg = int((want + ctas - 1) / ctas);
@@ -228,9 +230,8 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
   seg_len = (seg_len + v.chunk - 1) / v.chunk * v.chunk;
   nseg = (L + seg_len - 1) / seg_len;  // every segment non-empty
 
-  const int cb = kScanThreads / lpc;
   const bool x_ok = ((long long)dim * es) % 16 == 0 && aligned16(u) && aligned16(delta) && (!z || aligned16(z)) &&
-                    (cb * es) % 16 == 0;
+                    (v.cb * es) % 16 == 0;
   const bool bc_ok = ((long long)N * es) % 16 == 0 && aligned16(Bp) && aligned16(Cp);
   const int use_tma = knobs ? knobs->use_tma : 0;
   if (use_tma == 1 && !(x_ok && bc_ok))
@@ -239,6 +240,7 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
                 "dim*%d and dstate*%d multiples of 16 bytes)", es, es);
   plan->npl = npl;
   plan->lpc = lpc;
+  plan->cb = v.cb;
   plan->nseg = nseg;
   plan->seg_len = seg_len;
   plan->chunk = v.chunk;
@@ -247,14 +249,24 @@ mamba_status_t make_plan(int dtype, int batch, int dim, int N, int L, const mamb
   return MAMBA_OK;
 }
 
+// Wait limit (ns) the next scan and decode launches give their first
+// mbarrier waits; mamba_set_wait_limit_ns changes it (a test setting).
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitNsDefault};
+
 // The scan entry points' common body. conv_w == nullptr: u is the scan input;
 // otherwise u holds the conv input x and the kernels compute
 // u = SiLU(causal conv1d(x; conv_w, conv_b)) on the fly.
+//
+// static_scratch: NULL for the regular entry points, whose split-sequence
+// workspace comes from cudaMallocAsync on the call's stream; otherwise the
+// device address of a static array of static_bytes bytes that the workspace
+// must fit in (the allocation-free entry point), and nothing is allocated.
 mamba_status_t scan_fwd_impl(int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, const void* u,
                              const void* delta, const float* A_log, const void* B, const void* C, const float* D,
                              const void* z, const float* delta_bias, const float* initial_state, void* out,
                              float* last_state, const mamba_scan_plan_t* plan_knobs, mamba_stream_t stream_,
-                             const float* conv_w, const float* conv_b, int conv_width) {
+                             const float* conv_w, const float* conv_b, int conv_width, float* static_scratch = nullptr,
+                             size_t static_bytes = 0) {
   t_detail.clear();
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (batch < 0 || dim < 0 || seqlen < 0)
@@ -308,9 +320,16 @@ mamba_status_t scan_fwd_impl(int batch, int dim, int dstate, int seqlen, mamba_d
   st = make_plan(dtype, batch, dim, dstate, seqlen, plan_knobs, di.sms, u, delta, z, B, C, &plan);
   if (st != MAMBA_OK) return st;
 
+  const size_t ws_rows = (size_t)batch * (plan.nseg - 1) * dim;
+  const size_t ws_bytes = ws_rows * (dstate + 1) * sizeof(float);
+  if (static_scratch && ws_bytes > static_bytes)
+    return fail(MAMBA_ERR_UNSUPPORTED,
+                "the plan (%d segments) needs %zu bytes of scratch; the static scratch holds %zu bytes "
+                "(use fewer segments)", plan.nseg, ws_bytes, static_bytes);
+
   ScanMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  const uint32_t cb = uint32_t(kScanThreads / plan.lpc);
+  const uint32_t cb = uint32_t(plan.cb);
   if (plan.tma_x) {
     const uint32_t urows = plan.chunk + (conv_w ? 3 : 0);  // the fused conv reads 3 steps before the chunk
     if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, urows)) != MAMBA_OK) return st;
@@ -347,23 +366,26 @@ mamba_status_t scan_fwd_impl(int batch, int dim, int dstate, int seqlen, mamba_d
   a.conv_w = conv_w;
   a.conv_b = conv_w ? conv_b : nullptr;
   a.conv_width = conv_w ? conv_width : 0;
+  a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
 
   auto launch = [&](ScanMode mode, unsigned nz) {
     dim3 grid((dim + cb - 1) / cb, batch, nz);
     return launch_scan_pass(dtype, disc, plan.npl, plan.lpc, mode, a, maps, grid, stream);
   };
 
-  void* work = nullptr;
+  void* work = nullptr;  // the workspace when it is allocated here
   if (plan.nseg > 1) {
-    const size_t rows = (size_t)batch * (plan.nseg - 1) * dim;
-    const size_t bytes = rows * (dstate + 1) * sizeof(float);
-    cudaError_t e = cudaMallocAsync(&work, bytes, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(split-sequence workspace)");
-    a.agg_h = static_cast<float*>(work);
-    a.agg_dsum = a.agg_h + rows * dstate;
-    e = launch(ScanMode::kAggregate, plan.nseg - 1);
+    float* ws = static_scratch;  // every value is written by the aggregate pass before the full pass reads it
+    if (!ws) {
+      cudaError_t e = cudaMallocAsync(&work, ws_bytes, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(split-sequence workspace)");
+      ws = static_cast<float*>(work);
+    }
+    a.agg_h = ws;
+    a.agg_dsum = ws + ws_rows * dstate;
+    cudaError_t e = launch(ScanMode::kAggregate, plan.nseg - 1);
     if (e != cudaSuccess) {
-      cudaFreeAsync(work, stream);
+      if (work) cudaFreeAsync(work, stream);
       return cuda_fail(e, "scan aggregate pass launch");
     }
   }
@@ -488,6 +510,7 @@ mamba_status_t mamba_selective_state_update_ex(int batch, int dim, int dstate, m
   if (st != MAMBA_OK) return st;
   a.status = di.status;
   a.sms = di.sms;
+  a.wait_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   cudaError_t e = launch_state_update(in_dtype == MAMBA_F32 ? 0 : 1, a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "state update launch");
   return MAMBA_OK;
@@ -689,6 +712,10 @@ mamba_status_t mamba_device_status(int* status_out, mamba_stream_t stream_) {
 
 int mamba_version(void) { return kVersion; }
 
+unsigned long long mamba_set_wait_limit_ns(unsigned long long limit_ns) {
+  return g_wait_limit_ns.exchange(limit_ns);
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -722,107 +749,12 @@ extern "C" mamba_status_t mamba_selective_scan_fwd_noalloc(
     int batch, int dim, int dstate, int seqlen, mamba_dtype_t in_dtype, const void* u, const void* delta,
     const float* A_log, const void* B, const void* C, const float* D, const void* z, const float* delta_bias,
     const float* initial_state, void* out, float* last_state, const mamba_scan_plan_t* plan_knobs,
-    mamba_stream_t stream_) {
+    mamba_stream_t stream) {
   t_detail.clear();
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-  if (batch < 0 || dim < 0 || seqlen < 0)
-    return fail(MAMBA_ERR_INVALID_ARG, "negative size (batch=%d dim=%d seqlen=%d)", batch, dim, seqlen);
-  if (dstate < 1) return fail(MAMBA_ERR_INVALID_ARG, "dstate=%d must be >= 1", dstate);
-  if (dstate > kMaxState) return fail(MAMBA_ERR_UNSUPPORTED, "dstate=%d exceeds %d", dstate, kMaxState);
-  if (in_dtype != MAMBA_F32 && in_dtype != MAMBA_BF16)
-    return fail(MAMBA_ERR_INVALID_ARG, "unknown in_dtype %d", int(in_dtype));
-  if (batch > 65535) return fail(MAMBA_ERR_UNSUPPORTED, "batch=%d exceeds 65535", batch);
-  if (plan_knobs && (plan_knobs->lanes_per_channel < 0 || plan_knobs->segments < 0 || plan_knobs->use_tma < 0 ||
-                     plan_knobs->use_tma > 2 || plan_knobs->discretization < 0 || plan_knobs->discretization > 1))
-    return fail(MAMBA_ERR_INVALID_ARG, "negative or unknown plan knob");
-  const int disc = plan_knobs ? plan_knobs->discretization : 0;
-  if (batch == 0 || dim == 0) return MAMBA_OK;
-  const int dtype = in_dtype == MAMBA_F32 ? 0 : 1;
-  const size_t es = dtype == 0 ? 4 : 2;
-  const size_t n_state = (size_t)batch * dim * dstate;
-  if (!A_log) return fail(MAMBA_ERR_INVALID_ARG, "A_log is NULL");
-  if (seqlen == 0) {
-    if (last_state) {
-      cudaError_t e = initial_state
-                          ? cudaMemcpyAsync(last_state, initial_state, n_state * 4, cudaMemcpyDeviceToDevice, stream)
-                          : cudaMemsetAsync(last_state, 0, n_state * 4, stream);
-      if (e != cudaSuccess) return cuda_fail(e, "empty-sequence last_state");
-    }
-    return MAMBA_OK;
-  }
-  if (!u || !delta || !B || !C || !out)
-    return fail(MAMBA_ERR_INVALID_ARG, "a required pointer is NULL (u=%p delta=%p B=%p C=%p out=%p)", u, delta, B, C,
-                out);
-  const size_t nx = (size_t)batch * seqlen * dim * es;
-  const size_t nbc = (size_t)batch * seqlen * dstate * es;
-  const void* inputs[] = {u, delta, z, B, C, A_log, D, delta_bias, initial_state};
-  const size_t sizes[] = {nx, nx, nx, nbc, nbc, (size_t)dim * dstate * 4, (size_t)dim * 4, (size_t)dim * 4,
-                          n_state * 4};
-  for (int i = 0; i < 9; ++i) {
-    if (overlaps(out, nx, inputs[i], sizes[i])) return fail(MAMBA_ERR_INVALID_ARG, "out aliases input %d", i);
-    if (overlaps(last_state, n_state * 4, inputs[i], sizes[i]))
-      return fail(MAMBA_ERR_INVALID_ARG, "last_state aliases input %d", i);
-  }
-  if (overlaps(out, nx, last_state, n_state * 4)) return fail(MAMBA_ERR_INVALID_ARG, "out aliases last_state");
-
-  DeviceInfo di;
-  mamba_status_t st = device_info(&di);
-  if (st != MAMBA_OK) return st;
   float* scratch = nullptr;
-  if ((st = noalloc_scratch(&scratch)) != MAMBA_OK) return st;
-  Plan plan;
-  st = make_plan(dtype, batch, dim, dstate, seqlen, plan_knobs, di.sms, u, delta, z, B, C, &plan);
+  const mamba_status_t st = noalloc_scratch(&scratch);
   if (st != MAMBA_OK) return st;
-  const size_t rows = (size_t)batch * (plan.nseg - 1) * dim;
-  const size_t need = rows * (dstate + 1) * sizeof(float);
-  if (need > MAMBA_NOALLOC_SCRATCH_BYTES)
-    return fail(MAMBA_ERR_UNSUPPORTED,
-                "the plan (%d segments) needs %zu bytes of scratch; the static scratch holds %u bytes "
-                "(use fewer segments)", plan.nseg, need, MAMBA_NOALLOC_SCRATCH_BYTES);
-
-  ScanMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  const uint32_t cb = uint32_t(kScanThreads / plan.lpc);
-  if (plan.tma_x) {
-    if ((st = encode_3d(&maps.u, u, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
-    if ((st = encode_3d(&maps.delta, delta, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
-    if (z && (st = encode_3d(&maps.z, z, int(es), dim, seqlen, batch, cb, plan.chunk)) != MAMBA_OK) return st;
-  }
-  if (plan.tma_bc) {
-    if ((st = encode_3d(&maps.B, B, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
-    if ((st = encode_3d(&maps.C, C, int(es), dstate, seqlen, batch, dstate, plan.chunk)) != MAMBA_OK) return st;
-  }
-  ScanArgs a;
-  std::memset(&a, 0, sizeof(a));
-  a.batch = batch;
-  a.dim = dim;
-  a.dstate = dstate;
-  a.seqlen = seqlen;
-  a.nseg = plan.nseg;
-  a.seg_len = plan.seg_len;
-  a.u = u;
-  a.delta = delta;
-  a.z = z;
-  a.B = B;
-  a.C = C;
-  a.A_log = A_log;
-  a.D = D;
-  a.delta_bias = delta_bias;
-  a.h0 = initial_state;
-  a.out = out;
-  a.last_state = last_state;
-  a.tma_x = plan.tma_x;
-  a.tma_bc = plan.tma_bc;
-  a.status = di.status;
-  a.agg_h = scratch;                      // every value is written by the aggregate pass
-  a.agg_dsum = scratch + rows * dstate;   // before the full pass reads it
-  auto launch = [&](ScanMode mode, unsigned nz) {
-    dim3 grid((dim + cb - 1) / cb, batch, nz);
-    return launch_scan_pass(dtype, disc, plan.npl, plan.lpc, mode, a, maps, grid, stream);
-  };
-  cudaError_t e = cudaSuccess;
-  if (plan.nseg > 1) e = launch(ScanMode::kAggregate, plan.nseg - 1);
-  if (e == cudaSuccess) e = launch(ScanMode::kFull, plan.nseg);
-  if (e != cudaSuccess) return cuda_fail(e, "scan launch (no-alloc entry point)");
-  return MAMBA_OK;
+  return scan_fwd_impl(batch, dim, dstate, seqlen, in_dtype, u, delta, A_log, B, C, D, z, delta_bias, initial_state,
+                       out, last_state, plan_knobs, stream, nullptr, nullptr, 0, scratch,
+                       MAMBA_NOALLOC_SCRATCH_BYTES);
 }

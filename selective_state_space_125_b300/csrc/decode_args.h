@@ -22,6 +22,7 @@ struct DecodeArgs {
   int disc;     // 0 = zero-order hold, 1 = simplified Bbar = dt B
   int* status;  // device status word (see record_status)
   int sms;      // multiprocessors of the device
+  unsigned long long wait_ns;  // limit of the bulk kernel's first mbarrier waits (ns); 0 gives up at once
 };
 cudaError_t launch_state_update(int dtype, const DecodeArgs& a, cudaStream_t stream);
 

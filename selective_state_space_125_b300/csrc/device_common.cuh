@@ -15,9 +15,23 @@ namespace mamba {
 // returns early.
 constexpr int kStatusTimeout = 4;
 
-// Upper bound of every spin-wait in the kernels, in nanoseconds of
-// %globaltimer (2 s; a healthy wait is microseconds).
+// Default upper bound of every spin-wait in the kernels, in nanoseconds of
+// %globaltimer (2 s; a healthy wait is microseconds). The scan and decode
+// launches carry the limit of their first waits in their arguments, so that a
+// test can shorten it; the waits that drain copies in flight after a timeout
+// always use this default.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// |A| floor of the kernels. exp(dt A) and (exp(dt A) - 1) / A at |A| = 1e-20
+// equal their A -> 0 limits (1 and dt) in fp32 for any dt below 1e12, and
+// 1e-20 keeps A h, dt A and 1 / A inside the normal fp32 range.
+constexpr float kMinAbsA = 1e-20f;
+
+// Smallest |dt A| (natural units) at which the bf16 path forms exp(dt A) - 1
+// as ex2(dt A log2 e) - 1. The MUFU result carries an absolute error near
+// 2^-23, so the relative error of the difference is below 2^-9 there; steps
+// with a smaller |dt A| in any lane of the warp take expm1_acc instead.
+constexpr float kFastMinDtA = 6.103515625e-05f;  // 2^-14
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -61,6 +75,16 @@ __device__ __forceinline__ float softplus_fast(float x) {
 }
 __device__ __forceinline__ float softplus_precise(float x) {
   return fmaxf(x, 0.0f) + log1pf(expf(-fabsf(x)));
+}
+
+// exp(x) - 1 for x <= 0 with full relative accuracy, given xl = x log2(e)
+// and e = ex2(xl) (a MUFU value): the series x (1 + x/2 + x^2/6 + x^3/24)
+// below |x| = 1/8 (truncation error below x^4 / 120 < 2e-6 relative), e - 1
+// above it (cancellation error below 2^-23 / (1/8) = 1e-6 relative).
+__device__ __forceinline__ float expm1_acc(float xl, float e) {
+  const float x = xl * kLn2;
+  const float s = x * fmaf(x, fmaf(x, fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
+  return (fabsf(x) < 0.125f) ? s : e - 1.0f;
 }
 
 // SiLU(z) = z * sigmoid(z).
@@ -112,13 +136,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false once limit_ns
+// has passed. A limit of 0 gives up at once without polling (a test setting).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

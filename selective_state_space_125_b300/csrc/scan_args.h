@@ -8,7 +8,6 @@
 namespace mamba {
 
 constexpr int kScanThreads = 128;   // threads per CTA of the scan kernels
-constexpr int kScanStages = 3;      // TMA pipeline depth (time chunks in flight)
 
 struct ScanArgs {
   int batch, dim, dstate, seqlen;
@@ -33,6 +32,7 @@ struct ScanArgs {
   const float* conv_w;      // (D, conv_width): fused causal conv1d taps (conv variants only)
   const float* conv_b;      // (D) or null
   int conv_width;           // 1..4
+  unsigned long long wait_ns;  // limit of the pipeline's mbarrier waits (ns); 0 gives up at once
 };
 
 struct ScanMaps {
@@ -43,6 +43,7 @@ struct ScanMaps {
 struct ScanVariant {
   int npl;     // states per thread
   int lpc;     // threads per channel
+  int cb;      // channels per CTA
   int chunk;   // time steps per pipeline stage
   size_t smem_bytes;
 };

@@ -30,8 +30,18 @@
 // batch (dA_log, dD, ddelta_bias) are added with one atomic per thread at the end.
 //
 // Math: bf16 inputs use MUFU ex2/rcp and keep the scaled state s = A h during
-// the recomputation (s_t = abar (s_{t-1} + B u) - B u, so A h_{t-1} is read
-// directly); fp32 inputs use expm1f and the unscaled h, as the forward does.
+// the recomputation (s_t = s_{t-1} + (abar - 1)(s_{t-1} + B u), so A h_{t-1} is
+// read directly); fp32 inputs use expm1f and the unscaled h, as the forward
+// does. Where dt |A| is small, abar - 1 formed as ex2 - 1, and the dA_log
+// term dt abar lambda v - q lambda B u (whose two parts agree to first order in
+// dt A), lose their leading digits. So, as in the forward, a step whose warp
+// holds a state with dt |A| < 2^-12 takes the accurate form instead (a
+// warp-uniform branch; fp32 inputs always do): abar - 1 from expm1_acc, and
+//   dA_log = A sum_t lambda_t dt_t (abar h_{t-1} + dt_t phi'(dt A) B u),
+// phi(x) = (e^x - 1) / x, phi'(x) = (x e^x - e^x + 1) / x^2 from its series below
+// |x| = 1/8 (the A factor is taken out so that |A| below the kernels' 1e-20
+// floor still gives the exact dA_log). dA_log sums the fast and accurate
+// parts.
 //
 // Time segments (for small batch x channels over long sequences): the
 // sequence is cut into S segments of whole chunks, one CTA per (channel
@@ -174,16 +184,19 @@ __device__ __forceinline__ float2 ex2_2(float2 x) { return make_float2(hw_ex2(x.
 
 // ---------------------------------------------------- forward step (4 states)
 // bf16 inputs: scaled state s = A h in two packed pairs; Al = A log2(e).
-template <int DISC>
+template <int DISC, bool ACC>
 __device__ __forceinline__ void fwd_step_fast(float2 (&s)[2], float4 B4, float dt, float uu, const float2 (&Al)[2],
                                               const float2 (&A)[2]) {
-  const float2 dd = dup2(dt), u2 = dup2(uu), nu = dup2(-uu);
+  const float2 dd = dup2(dt), u2 = dup2(uu);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
-    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    const float2 x = __fmul2_rn(dd, Al[h]);
+    const float2 ab = ex2_2(x);
     if (DISC == 0) {
-      s[h] = __ffma2_rn(ab, __ffma2_rn(Bp, u2, s[h]), __fmul2_rn(Bp, nu));  // abar (s + B u) - B u
+      const float2 em1 = ACC ? make_float2(expm1_acc(x.x, ab.x), expm1_acc(x.y, ab.y))
+                             : __fadd2_rn(ab, make_float2(-1.f, -1.f));
+      s[h] = __ffma2_rn(em1, __ffma2_rn(Bp, u2, s[h]), s[h]);  // s + (abar - 1)(s + B u)
     } else {
       s[h] = __ffma2_rn(ab, s[h], __fmul2_rn(__fmul2_rn(A[h], dd), __fmul2_rn(Bp, u2)));  // abar s + A dt B u
     }
@@ -203,18 +216,31 @@ __device__ __forceinline__ void fwd_step_precise(float (&h)[4], float4 B4, float
   }
 }
 
+// phi'(x) for phi(x) = (e^x - 1) / x, x <= 0, given xl = x log2(e), e = e^x,
+// em1 = e^x - 1 (accurate) and ix = 1 / x: the series 1/2 + x/3 + x^2/8 + x^3/30
+// below |x| = 1/8 (truncation error below x^4 / 144 / (1/2) < 6e-7 relative),
+// (e - em1 ix) ix above it.
+__device__ __forceinline__ float dphi_acc(float xl, float e, float em1, float ix) {
+  const float x = xl * kLn2;
+  const float ser = fmaf(x, fmaf(x, fmaf(x, 1.0f / 30.0f, 1.0f / 8.0f), 1.0f / 3.0f), 0.5f);
+  return (fabsf(x) < 0.125f) ? ser : (e - em1 * ix) * ix;
+}
+
 // ---------------------------------------------------- adjoint step (4 states)
 // Given s_t (sn), s_{t-1} (sp) and lambda_{t+1} abar_{t+1} (carry): updates
 // carry to abar_t lambda_t, adds the dA_log terms, writes the dB partials to
 // v[0..3] and the dC partials to v[4..7], and returns the sums over the 4
 // states of the du, dt and y terms.
-template <int DISC>
+// ACC = false: abar - 1 = ex2 - 1 and the dA_log terms in dApos - dAneg;
+// ACC = true: expm1_acc, and the dA_log terms (without their A factor) in G.
+template <int DISC, bool ACC>
 __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, float4 C4, float dt, float uu, float dy,
                                               float2 (&carry)[2], float2 (&dApos)[2], float2 (&dAneg)[2],
-                                              const float2 (&Al)[2], const float2 (&Ik)[2], float (&v)[8],
-                                              float& dus, float& ddt, float& ys) {
+                                              float2 (&G)[2], const float2 (&Al)[2], const float2 (&Ik)[2],
+                                              float (&v)[8], float& dus, float& ddt, float& ys) {
   const float2 dd = dup2(dt), u2 = dup2(uu), yy = dup2(dy);
   float2 sdus = make_float2(0.f, 0.f), sddt = sdus, sys = sdus;
+  [[maybe_unused]] const float rdt = ACC ? hw_rcp(dt) : 0.0f;  // 1 / dt (dt = 0 only where |x| < 1/8)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
@@ -225,20 +251,31 @@ __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, f
     const float2 ht = __fmul2_rn(snp, Ik[h]);
     const float2 dc = __fmul2_rn(yy, ht);
     sys = __ffma2_rn(Cp, ht, sys);
-    const float2 ab = ex2_2(__fmul2_rn(dd, Al[h]));
+    const float2 x = __fmul2_rn(dd, Al[h]);
+    const float2 ab = ex2_2(x);
     const float2 Bu = __fmul2_rn(Bp, u2);
     const float2 al = __fmul2_rn(ab, lam);
     float2 r, m;
     if (DISC == 0) {
-      const float2 q = __fmul2_rn(__fadd2_rn(ab, make_float2(-1.f, -1.f)), Ik[h]);  // (abar - 1) / A
+      const float2 em1 = ACC ? make_float2(expm1_acc(x.x, ab.x), expm1_acc(x.y, ab.y))
+                             : __fadd2_rn(ab, make_float2(-1.f, -1.f));
+      const float2 q = __fmul2_rn(em1, Ik[h]);                 // (abar - 1) / A
       r = __fmul2_rn(lam, q);
       m = __fmul2_rn(al, __fadd2_rn(spp, Bu));                  // abar lambda (A h_{t-1} + B u)
-      dApos[h] = __ffma2_rn(dd, m, dApos[h]);                   // + dt abar lambda v
-      dAneg[h] = __ffma2_rn(r, Bu, dAneg[h]);                   // - q lambda B u
+      if constexpr (ACC) {
+        const float2 ix = __fmul2_rn(Ik[h], dup2(rdt));         // 1 / (dt A)
+        const float2 dp = make_float2(dphi_acc(x.x, ab.x, em1.x, ix.x), dphi_acc(x.y, ab.y, em1.y, ix.y));
+        const float2 hp = __fmul2_rn(spp, Ik[h]);               // h_{t-1}
+        const float2 inner = __ffma2_rn(al, hp, __fmul2_rn(__fmul2_rn(dd, dp), __fmul2_rn(lam, Bu)));
+        G[h] = __ffma2_rn(dd, inner, G[h]);                     // dt (abar h + dt phi' B u) lambda
+      } else {
+        dApos[h] = __ffma2_rn(dd, m, dApos[h]);                 // + dt abar lambda v
+        dAneg[h] = __ffma2_rn(r, Bu, dAneg[h]);                 // - q lambda B u
+      }
     } else {
       r = __fmul2_rn(lam, dd);
       m = __ffma2_rn(al, spp, __fmul2_rn(lam, Bu));             // lambda (abar A h_{t-1} + B u)
-      dApos[h] = __ffma2_rn(__fmul2_rn(dd, al), spp, dApos[h]); // + dt abar lambda A h_{t-1}
+      G[h] = __ffma2_rn(__fmul2_rn(dd, al), __fmul2_rn(spp, Ik[h]), G[h]);  // dt abar lambda h_{t-1}
     }
     const float2 db = __fmul2_rn(r, u2);
     sdus = __ffma2_rn(r, Bp, sdus);
@@ -254,6 +291,7 @@ __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, f
   ys = sys.x + sys.y;
 }
 
+// dAl collects the dA_log terms without their A factor (multiplied in at the end).
 template <int DISC>
 __device__ __forceinline__ void adj_step_precise(float4 sn4, float4 sp4, float4 B4, float4 C4, float dt, float uu,
                                                  float dy, float (&carry)[4], float (&dAl)[4], const float (&A)[4],
@@ -274,14 +312,17 @@ __device__ __forceinline__ void adj_step_precise(float4 sn4, float4 sp4, float4 
     const float al = ab * lam;
     float r, m;
     if (DISC == 0) {
+      const float x = dt * A[k];
+      // phi'(x) = (x e^x - e^x + 1) / x^2: series below |x| = 1/8, closed form above
+      const float dp = (fabsf(x) < 0.125f) ? fmaf(x, fmaf(x, fmaf(x, 1.0f / 30.0f, 1.0f / 8.0f), 1.0f / 3.0f), 0.5f)
+                                           : (ab - e / x) / x;
       r = lam * (e * Ik[k]);
       m = al * (Ahp + Bu);
-      dAl[k] = fmaf(dt, m, dAl[k]);
-      dAl[k] = fmaf(-r, Bu, dAl[k]);
+      dAl[k] = fmaf(dt, fmaf(al, sp[k], dt * dp * lam * Bu), dAl[k]);  // dt (abar h + dt phi' B u) lambda
     } else {
       r = lam * dt;
       m = fmaf(al, Ahp, lam * Bu);
-      dAl[k] = fmaf(dt * al, Ahp, dAl[k]);
+      dAl[k] = fmaf(dt * al, sp[k], dAl[k]);                               // dt abar lambda h_{t-1}
     }
     ddt += m;
     v[k] = r * uu;
@@ -344,20 +385,23 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     ch_D[tid] = (ok && a.D) ? a.D[d0 + tid] : 0.0f;
   }
 
-  // A = -exp(A_log), 1/A and (fast path) A log2(e) for my states.
-  float A[NPL], Ik[NPL];
+  // A = -exp(A_log) with |A| >= kMinAbsA, 1/A and (fast path) A log2(e) for my
+  // states; Atrue keeps A unfloored for the final dA_log = A dloss/dA.
+  float A[NPL], Ik[NPL], Atrue[NPL];
   float2 A2[2], Al2[2], Ik2[2];
+  float minA = 3.0e38f;  // smallest |A| of my channel's states
 #pragma unroll
   for (int k = 0; k < NPL; ++k) {
     const float al = cv ? a.A_log[(size_t)d * N + n0 + k] : 0.0f;
-    if constexpr (PRECISE) {
-      A[k] = -expf(al);
-      Ik[k] = 1.0f / A[k];
-    } else {
-      A[k] = -hw_ex2(al * kLog2e);
-      Ik[k] = hw_rcp(A[k]);
-    }
+    Atrue[k] = PRECISE ? -expf(al) : -hw_ex2(al * kLog2e);
+    A[k] = fminf(Atrue[k], -kMinAbsA);
+    Ik[k] = PRECISE ? 1.0f / A[k] : hw_rcp(A[k]);
+    minA = fminf(minA, -A[k]);
   }
+#pragma unroll
+  for (int o = 1; o < LPC; o <<= 1) minA = fminf(minA, __shfl_xor_sync(0xffffffffu, minA, o));
+  // dt below which a step of my channel needs the accurate form (bf16 inputs)
+  const float thr = kBwdFastMinDtA / minA;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     A2[h] = make_float2(A[2 * h], A[2 * h + 1]);
@@ -384,9 +428,17 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
     else return make_float4(s2[0].x * Ik[0], s2[0].y * Ik[1], s2[1].x * Ik[2], s2[1].y * Ik[3]);
   };
+  // One forward step; the fast bf16 form unless a lane of the warp has
+  // dt |A| < 2^-12 (a warp-uniform choice; dt = 0 marks steps past the end).
   auto fwd_step = [&](float4 B4, float dt, float uu) {
-    if constexpr (PRECISE) fwd_step_precise<DISC>(hs, B4, dt, uu, A, Ik);
-    else fwd_step_fast<DISC>(s2, B4, dt, uu, Al2, A2);
+    if constexpr (PRECISE) {
+      fwd_step_precise<DISC>(hs, B4, dt, uu, A, Ik);
+    } else {
+      if (__all_sync(0xffffffffu, dt >= thr || dt == 0.0f))
+        fwd_step_fast<DISC, false>(s2, B4, dt, uu, Al2, A2);
+      else
+        fwd_step_fast<DISC, true>(s2, B4, dt, uu, Al2, A2);
+    }
   };
 
   // Exponential decay of my states over a segment with the given sum of dt.
@@ -458,8 +510,8 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   }
 
   // --------------------------------------------------- phase 2: adjoint
-  float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs
-  float2 carry2[2], dApos[2], dAneg[2];               // bf16 inputs
+  float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs (dAl: without the A factor)
+  float2 carry2[2], dApos[2], dAneg[2], G2[2];        // bf16 inputs (G2: accurate terms, without A)
   {
     float4 g = (MODE == kBwdFull && cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
     if constexpr (MODE == kBwdFull) {
@@ -474,7 +526,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
     carry2[0] = lo2(g);
     carry2[1] = hi2(g);  // (kBwdAdjAgg runs on the scalar carry for either input type)
-    dApos[0] = dApos[1] = dAneg[0] = dAneg[1] = make_float2(0.f, 0.f);
+    dApos[0] = dApos[1] = dAneg[0] = dAneg[1] = G2[0] = G2[1] = make_float2(0.f, 0.f);
   }
   float dD_acc = 0.0f, dbias_acc = 0.0f;  // channel d0 + tid % CB
   XCopy4 xq;
@@ -576,8 +628,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
           const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
           if constexpr (PRECISE)
             adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
+          else if (__all_sync(0xffffffffu, tc.x >= thr))
+            adj_step_fast<DISC, false>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, G2, Al2, Ik2, v, dus,
+                                       ddt, ys);
           else
-            adj_step_fast<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, Al2, Ik2, v, dus, ddt, ys);
+            adj_step_fast<DISC, true>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, G2, Al2, Ik2, v, dus,
+                                      ddt, ys);
           sn = sp;
         }
 #pragma unroll
@@ -651,11 +707,11 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   if (cv) {
     float4 dA4, g4;
     if constexpr (PRECISE) {
-      dA4 = make_float4(dAl[0], dAl[1], dAl[2], dAl[3]);
+      dA4 = make_float4(Atrue[0] * dAl[0], Atrue[1] * dAl[1], Atrue[2] * dAl[2], Atrue[3] * dAl[3]);
       g4 = make_float4(carry[0], carry[1], carry[2], carry[3]);
     } else {
-      dA4 = make_float4(dApos[0].x - dAneg[0].x, dApos[0].y - dAneg[0].y, dApos[1].x - dAneg[1].x,
-                        dApos[1].y - dAneg[1].y);
+      dA4 = make_float4(fmaf(Atrue[0], G2[0].x, dApos[0].x - dAneg[0].x), fmaf(Atrue[1], G2[0].y, dApos[0].y - dAneg[0].y),
+                        fmaf(Atrue[2], G2[1].x, dApos[1].x - dAneg[1].x), fmaf(Atrue[3], G2[1].y, dApos[1].y - dAneg[1].y));
       g4 = make_float4(carry2[0].x, carry2[0].y, carry2[1].x, carry2[1].y);
     }
     atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), dA4);

@@ -15,7 +15,7 @@
 //     zeros);
 //   - time is walked in chunks of kChunk steps. Thread 0 stages each chunk's
 //     u / delta / z tiles ([chunk][channels]) and B / C tiles ([chunk][N])
-//     into shared memory with 3-D TMA loads, kScanStages chunks ahead,
+//     into shared memory with 3-D TMA loads, kStages chunks ahead,
 //     completing on one mbarrier per stage. When the layout does not meet
 //     TMA's 16-byte rules the CTA fills the same tiles with plain loads;
 //   - per chunk the CTA widens the B / C tiles to fp32 once for all of its
@@ -27,10 +27,20 @@
 //     holds the full y of step q, adds D u, applies the SiLU gate and stores
 //     it. With LPC == 1 a thread does all of this for its own channel;
 //   - bf16 inputs use the fast path: a scaled state s = A h, so that one step
-//     is s <- Abar (s + B u) - B u, and y = sum (C / A) s, all on packed
-//     f32x2 FMUL/FFMA pairs of states, with Abar by MUFU ex2. fp32 inputs use
-//     the precise path on the unscaled state with expm1f, so that
-//     (Abar - 1) / A keeps full relative accuracy.
+//     is s <- s + (Abar - 1)(s + B u), and y = sum (C / A) s, all on packed
+//     f32x2 FMUL/FFMA pairs of states, with Abar by MUFU ex2 and Abar - 1 =
+//     ex2 - 1. Where dt |A| is small, ex2 - 1 loses the input term to
+//     cancellation (relative error near 2^-23 / |dt A|), so before each chunk
+//     the CTA checks its delta tile against a per-channel bound (the delta
+//     at which dt |A| = 2^-14 for the channel's smallest |A|): if some step
+//     of some channel falls below it, the whole chunk takes Abar - 1 from a
+//     short series instead (expm1_acc). The check rides on the chunk's
+//     barrier (__syncthreads_or), so the unrolled step loop carries no
+//     branch. |A| is floored at 1e-20, where Abar and (Abar - 1) / A equal
+//     their A -> 0 limits (1 and dt) in fp32 ("State Space Models and Mamba"
+//     §2, the zero-order hold's limit). fp32 inputs use the precise path on
+//     the unscaled state with expm1f, so that (Abar - 1) / A keeps full
+//     relative accuracy.
 //
 // With CONV the kernel also runs the step in front of the scan in the Mamba
 // block: u = SiLU(causal depthwise conv1d(x) + bias), width <= 4 ("Mamba"
@@ -68,15 +78,16 @@ struct ScanGeom {
   static constexpr int kNP = NPL * LPC;           // padded state count
   static constexpr int kES = int(sizeof(Tin));
   static constexpr int kChunk = 16;               // steps per pipeline stage (a multiple of LPC)
+  static constexpr int kStages = 3;               // TMA pipeline depth (chunks in flight)
   static constexpr int kURows = kChunk + (CONV ? kConvHalo : 0);  // rows of the u (or conv input) tile
   static constexpr size_t kUTile = scan_a128(size_t(kURows) * kCB * kES);
   static constexpr size_t kXTile = scan_a128(size_t(kChunk) * kCB * kES);
   static constexpr size_t kBCTile = scan_a128(size_t(kChunk) * kNP * kES);
   static constexpr size_t kStage = kUTile + 2 * kXTile + 2 * kBCTile;
   static constexpr size_t kBC32 = scan_a128(size_t(kChunk) * 2 * kNP * 4);  // [t][B | C][NP] fp32, x2 buffers
-  static constexpr size_t kChan = scan_a128(size_t(kCB) * 2 * 4);           // bias, D per channel
+  static constexpr size_t kChan = scan_a128(size_t(kCB) * 3 * 4);           // bias, D, delta bound per channel
   static constexpr size_t kBar = 128;
-  static constexpr size_t kOffBC32 = kScanStages * kStage;
+  static constexpr size_t kOffBC32 = kStages * kStage;
   static constexpr size_t kOffChan = kOffBC32 + 2 * kBC32;
   static constexpr size_t kOffBar = kOffChan + kChan;
   static constexpr size_t kSmem = kOffBar + kBar + 128;  // + alignment slack of the dynamic base
@@ -86,15 +97,16 @@ struct ScanGeom {
 };
 
 // One step of the fast path for NPL states held as NPL/2 packed pairs:
-// s <- Abar (s + B u) - B u with Abar = 2^(dt * Ak), and (READ) the partial
-// readout sum_j (C_j * Ik_j) s_j. Bt / Ct point at this thread's states.
-template <int NPL, bool READ>
+// s <- s + em1 (s + B u) with em1 = Abar - 1, Abar = 2^(dt * Ak), and (READ)
+// the partial readout sum_j (C_j * Ik_j) s_j. ACC selects how em1 is formed:
+// ex2 - 1 (false) or expm1_acc (true, exact to a few ulp at any dt A). Bt / Ct
+// point at this thread's states.
+template <int NPL, bool READ, bool ACC>
 __device__ __forceinline__ float step_fast(float2 (&s)[NPL / 2], const float2 (&Ak)[NPL / 2],
                                            const float2 (&Ik)[NPL / 2], float dt, float u, const float* Bt,
                                            const float* Ct) {
   const float2 dd = make_float2(dt, dt);
   const float2 uu = make_float2(u, u);
-  const float2 nu = make_float2(-u, -u);
   float2 yy[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};  // two chains of the readout sum
 #pragma unroll
   for (int j = 0; j < NPL / 2; j += 2) {
@@ -106,9 +118,12 @@ __device__ __forceinline__ float step_fast(float2 (&s)[NPL / 2], const float2 (&
       const float2 Bp = h == 0 ? make_float2(B4.x, B4.y) : make_float2(B4.z, B4.w);
       const float2 x = __fmul2_rn(dd, Ak[j + h]);
       const float2 ab = make_float2(hw_ex2(x.x), hw_ex2(x.y));
-      const float2 w = __ffma2_rn(Bp, uu, s[j + h]);
-      const float2 nv = __fmul2_rn(Bp, nu);
-      s[j + h] = __ffma2_rn(ab, w, nv);
+      float2 em1;
+      if constexpr (ACC)
+        em1 = make_float2(expm1_acc(x.x, ab.x), expm1_acc(x.y, ab.y));
+      else
+        em1 = __fadd2_rn(ab, make_float2(-1.0f, -1.0f));
+      s[j + h] = __ffma2_rn(em1, __ffma2_rn(Bp, uu, s[j + h]), s[j + h]);
       if (READ) {
         const float2 Cp = h == 0 ? make_float2(C4.x, C4.y) : make_float2(C4.z, C4.w);
         yy[h] = __ffma2_rn(__fmul2_rn(Cp, Ik[j + h]), s[j + h], yy[h]);
@@ -237,7 +252,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   using E = Elem<Tin>;
   constexpr bool PRECISE = std::is_same<Tin, float>::value;
   constexpr bool SCALED = !PRECISE && DISC == 0;  // fast ZOH path keeps s = A h
-  constexpr int CB = G::kCB, NP = G::kNP, CH = G::kChunk;
+  constexpr int CB = G::kCB, NP = G::kNP, CH = G::kChunk, NS = G::kStages;
   constexpr int NH = NPL / 2;
 
   extern __shared__ unsigned char smem_dyn[];
@@ -245,6 +260,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   float* chan_bias = reinterpret_cast<float*>(smem + G::kOffChan);
   float* chan_D = chan_bias + CB;
+  float* chan_dmin = chan_D + CB;  // delta at or above which a step of the channel may take the fast em1
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + G::kOffBar);
 
   // Stage s: u tile (kURows rows; with CONV its first kConvHalo rows are the
@@ -287,7 +303,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
 
   // Chunk staging by TMA (thread 0 only).
   auto issue = [&](int k) {
-    const int s = k % kScanStages;
+    const int s = k % NS;
     const int t0 = t_begin + k * CH;
     uint32_t bytes = 0;
     if (a.tma_x) bytes += uint32_t(((has_z ? 2 : 1) * CH + G::kURows) * CB * sizeof(Tin));
@@ -305,7 +321,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   };
 
   if (use_tma && tid == 0) {
-    for (int s = 0; s < kScanStages; ++s) mbar_init(&mbar[s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&mbar[s], 1);
     fence_mbar_init();
     if (a.tma_x) {
       prefetch_tensormap(&maps.u);
@@ -320,22 +336,25 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   __syncthreads();
   int issued = 0;  // chunks handed to TMA so far (thread 0)
   if (use_tma && tid == 0)
-    for (; issued < min(kScanStages, nchunks); ++issued) issue(issued);
+    for (; issued < min(NS, nchunks); ++issued) issue(issued);
 
   // Per-thread constants for my NPL states:
   //  fast:    Ak = A * log2(e) (exponent for ex2), Ik = 1 / A;
   //  precise: Ak = A,                              Ik = 1 / A (0 if A == 0).
   // Initial state: h0 (or 0), then the composed aggregates of earlier segments.
+  // A = -exp(A_log) with |A| >= kMinAbsA.
   float2 Ak[NH], Ik[NH], st[NH];
+  float minA = 3.0e38f;  // smallest |A| of my real states
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
     const int n = q * NPL + j;
     const bool real = n < N;
     float A = -1.0f;
     if (dvalid && real) A = -expf(a.A_log[(size_t)d * N + n]);
-    if (!PRECISE) A = fminf(A, -1e-30f);
+    A = fminf(A, -kMinAbsA);
+    if (real) minA = fminf(minA, -A);
     const float ak = real ? (PRECISE ? A : A * kLog2e) : 0.0f;
-    const float ik = (real && A != 0.0f) ? 1.0f / A : 0.0f;
+    const float ik = real ? 1.0f / A : 0.0f;
     float hin = 0.0f;
     if (!AGG && real && dvalid) {
       if (a.h0) hin = a.h0[((size_t)b * Dm + d) * N + n];
@@ -359,6 +378,17 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   }
   const float bias = chan_bias[c];
   const float Dd = chan_D[c];
+  if constexpr (SCALED) {
+    // The channel's delta bound: dt = softplus(delta + bias) >= kFastMinDtA / min|A|
+    // exactly when delta >= softplus^-1(kFastMinDtA / min|A|) - bias.
+#pragma unroll
+    for (int o = 1; o < LPC; o <<= 1) minA = fminf(minA, __shfl_xor_sync(0xffffffffu, minA, o));
+    if (q == 0) {
+      const float dtb = kFastMinDtA / minA;
+      chan_dmin[c] = (dtb > 20.0f ? dtb : logf(expm1f(dtb))) - bias;
+    }
+    __syncthreads();
+  }
   // Conv taps aligned to the u tile: tap j multiplies row tm + j (input step
   // t - kConvHalo + j), so a width-W kernel fills taps kConvHalo + 1 - W .. kConvHalo.
   float cw[kConvHalo + 1] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -379,7 +409,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   double dsum_d = 0.0;  // AGG: the same in fp64 (precise path)
 
   // The steps of one staged chunk (see the loop below).
-  auto run_chunk = [&]<bool HZ>(int s, int kc, int t0, int tv) {
+  auto run_chunk = [&]<bool HZ, bool ACC>(int s, int kc, int t0, int tv) {
     const Tin* su = xu(s) + c;
     const Tin* sd = xd(s) + c;
     const Tin* sz = xz(s) + c;
@@ -426,7 +456,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         else if constexpr (PRECISE)
           yp[j] = step_precise<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
         else
-          yp[j] = step_fast<NPL, !AGG>(st, Ak, Ik, dt, u, Bt, Bt + NP);
+          yp[j] = step_fast<NPL, !AGG, ACC>(st, Ak, Ik, dt, u, Bt, Bt + NP);
         if constexpr (AGG) {
           if (PRECISE) dsum_d += dt; else dsum += dt;
         }
@@ -451,17 +481,17 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   };
 
   for (int k = 0; k < nchunks; ++k) {
-    const int s = k % kScanStages;
+    const int s = k % NS;
     const int t0 = t_begin + k * CH;
     const int tv = min(CH, t_end - t0);
 
     if (use_tma) {
-      const bool ok = mbar_wait_bounded(&mbar[s], (k / kScanStages) & 1);
+      const bool ok = mbar_wait_bounded(&mbar[s], (k / NS) & 1, a.wait_ns);
       if (__syncthreads_or(!ok)) {
         if (tid == 0) {
           record_status(a.status, kStatusTimeout);
           // Let copies already in flight land before the CTA's shared memory goes away.
-          for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&mbar[kk % kScanStages], (kk / kScanStages) & 1);
+          for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&mbar[kk % NS], (kk / NS) & 1);
         }
         return;
       }
@@ -482,6 +512,32 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         xd(s)[i] = in ? gdl[off] : Tin(0.0f);
         if (has_z) xz(s)[i] = in ? gz[off] : Tin(0.0f);
       }
+      if constexpr (SCALED) __syncthreads();  // the delta check below reads other threads' rows
+    }
+    // Whether some channel of the CTA has a step in this chunk with dt |A|
+    // below kFastMinDtA: the CB/2 channel pairs x CH rows of the delta tile
+    // are split over the threads, RPT rows of one pair each (packed bf16
+    // pairs, a min tree); each thread compares its rows' smallest delta with
+    // its pair's bounds, and the chunk's barrier below ORs the answers over
+    // the CTA. The loads are issued here so that they overlap the widening.
+    bool slow = false;
+    if constexpr (SCALED) {
+      constexpr int PAIRS = CB / 2;
+      constexpr int RPT = (CH * PAIRS + kScanThreads - 1) / kScanThreads;  // rows per thread
+      const int p = tid % PAIRS, r0 = (tid / PAIRS) * RPT;
+      const __nv_bfloat162* col = reinterpret_cast<const __nv_bfloat162*>(xd(s)) + p;
+      const __nv_bfloat162 inf2 = __bfloat162bfloat162(__ushort_as_bfloat16(0x7F80u));
+      __nv_bfloat162 m[RPT];
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) m[i] = (r0 + i < tv) ? col[(r0 + i) * PAIRS] : inf2;
+#pragma unroll
+      for (int w = 1; w < RPT; w *= 2)
+#pragma unroll
+        for (int i = 0; i + w < RPT; i += 2 * w) m[i] = __hmin2(m[i], m[i + w]);
+      if (r0 < tv) {
+        const float2 mf = __bfloat1622float2(m[0]);
+        slow = mf.x < chan_dmin[2 * p] || mf.y < chan_dmin[2 * p + 1];
+      }
     }
     // B / C rows widened to fp32 once for every channel of the CTA (zero beyond N).
     float* bck = bc32(k);
@@ -501,7 +557,11 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       bck[t * 2 * NP + n] = bv;
       bck[t * 2 * NP + NP + n] = cv;
     }
-    __syncthreads();  // chunk k staged; every thread is past chunk k-1
+    if constexpr (SCALED) {
+      slow = __syncthreads_or(slow);  // chunk k staged; every thread is past chunk k-1
+    } else {
+      __syncthreads();  // chunk k staged; every thread is past chunk k-1
+    }
     if (use_tma && tid == 0 && k >= 1 && issued < nchunks) {
       fence_proxy_async_smem();  // chunk k-1's stage was read through the generic proxy
       issue(issued);
@@ -514,10 +574,17 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     // is (Abar = 1, no input), and store nothing. The loop is branch-free and
     // fully unrolled so that the compiler can overlap a group's recurrence
     // with the next group's softplus and the previous group's epilogue.
-    if (has_z)
-      run_chunk.template operator()<true>(s, k, t0, tv);
-    else
-      run_chunk.template operator()<false>(s, k, t0, tv);
+    if (slow) {
+      if (has_z)
+        run_chunk.template operator()<true, true>(s, k, t0, tv);
+      else
+        run_chunk.template operator()<false, true>(s, k, t0, tv);
+    } else {
+      if (has_z)
+        run_chunk.template operator()<true, false>(s, k, t0, tv);
+      else
+        run_chunk.template operator()<false, false>(s, k, t0, tv);
+    }
   }
 
   if (!dvalid) return;
@@ -571,6 +638,7 @@ void describe_variant(ScanVariant* v) {
   using G = ScanGeom<Tin, NPL, LPC>;
   v->npl = NPL;
   v->lpc = LPC;
+  v->cb = G::kCB;
   v->chunk = G::kChunk;
   v->smem_bytes = G::kSmem;
 }

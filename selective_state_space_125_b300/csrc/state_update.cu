@@ -17,13 +17,14 @@
 // warp shuffles.
 //
 // Math: bf16 inputs use MUFU ex2 for exp(A_log) and exp(dt A) and rcp for
-// 1/A. The register-path kernel takes exp(dt A) - 1 from a four-term series
-// when |dt A| < 1/8 (where ex2 - 1 would cancel) and from ex2 - 1 otherwise,
-// so (exp(dt A) - 1) / A keeps a relative error near 1e-6. The bulk-staged
-// kernel updates the scaled state A h in packed pairs, as the bf16 scan does
-// (s' = abar (s + B u) - B u): fewer instructions, and a relative error of the
-// input term near 2^-22 / |dt A|. fp32 inputs use expf / expm1f / log1pf.
-// With the simplified discretisation (disc = 1) the input term is dt B u.
+// 1/A. Both kernels take exp(dt A) - 1 from a four-term series when
+// |dt A| < 1/8 (where ex2 - 1 would cancel) and from ex2 - 1 otherwise
+// (expm1_acc), so (exp(dt A) - 1) / A keeps a relative error near 1e-6 at any
+// dt A. The bulk-staged kernel updates the scaled state A h in packed pairs:
+// s' = s + (exp(dt A) - 1)(s + B u), h' = s' / A. fp32 inputs use expf /
+// expm1f / log1pf. |A| is floored at 1e-20, where exp(dt A) and
+// (exp(dt A) - 1) / A equal their A -> 0 limits (1 and dt) in fp32. With the
+// simplified discretisation (disc = 1) the input term is dt B u.
 #include <algorithm>
 #include <type_traits>
 
@@ -34,14 +35,6 @@ namespace mamba {
 
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRows = 4;  // batch rows per thread, loaded together
-
-// exp(x) - 1 for x <= 0 from e = 2^(x log2 e) (a MUFU value of x): series
-// below |x| = 1/8 (truncation error < x^5 / 120, relative < 3e-7), e - 1
-// above (cancellation error 2^-23 / |x| < 1e-6).
-__device__ __forceinline__ float expm1_from_ex2(float x, float e) {
-  const float s = x * fmaf(x, fmaf(x, fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f), 1.0f);
-  return (fabsf(x) < 0.125f) ? s : e - 1.0f;
-}
 
 // Four consecutive B or C values of one batch row, loaded in one access and
 // widened on use: bf16 keeps the raw 8 bytes (two registers), fp32 a float4.
@@ -93,7 +86,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
     for (int i = 0; i < 4; ++i) {
       const int n = n0 + i;
       const float al = (dvalid && n < N) ? arow[n] : 0.0f;
-      const float A = PRECISE ? -expf(al) : -hw_ex2(al * kLog2e);
+      const float A = fminf(PRECISE ? -expf(al) : -hw_ex2(al * kLog2e), -kMinAbsA);
       Al[k][i] = PRECISE ? A : A * kLog2e;
       Ik[k][i] = PRECISE ? 1.0f / A : hw_rcp(A);
     }
@@ -178,7 +171,7 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
             ab = 1.0f + e;
           } else {
             ab = hw_ex2(x);
-            e = expm1_from_ex2(x * kLn2, ab);
+            e = expm1_acc(x, ab);
           }
           // (Abar - 1) / A, with the limit dt where dt A underflows to zero
           coef = (x != 0.0f) ? (PRECISE ? e / Al[k][i] : e * Ik[k][i]) : dt;
@@ -334,7 +327,7 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
 #pragma unroll
   for (int i = 0; i < kBulkFloats; ++i) {
     const float al = cvalid ? a.A_log[(size_t)d * N + n0 + i] : 0.0f;
-    Av[i] = PRECISE ? -expf(al) : -hw_ex2(al * kLog2e);
+    Av[i] = fminf(PRECISE ? -expf(al) : -hw_ex2(al * kLog2e), -kMinAbsA);
     Ik[i] = PRECISE ? 1.0f / Av[i] : hw_rcp(Av[i]);
   }
 #pragma unroll
@@ -349,7 +342,7 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
   for (int i = 0; i < nrows; ++i) {
     const int s = i % S;
     const int b = int(blockIdx.y) + i * rb;
-    const bool ok = mbar_wait_bounded(&full[s], (i / S) & 1);
+    const bool ok = mbar_wait_bounded(&full[s], (i / S) & 1, a.wait_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
         record_status(a.status, kStatusTimeout);
@@ -379,9 +372,9 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
           y = fmaf(Cv[k], hv[k], y);
         }
       } else {
-        // bf16: packed pairs. Zero-order hold on the scaled state s = A h, as in the
-        // scan: s' = abar (s + B u) - B u, h' = s' / A.
-        const float2 dd = make_float2(dt, dt), uu = make_float2(uf, uf), nu = make_float2(-uf, -uf);
+        // bf16: packed pairs. Zero-order hold on the scaled state s = A h:
+        // s' = s + (abar - 1)(s + B u), h' = s' / A, with abar - 1 accurate at any dt A.
+        const float2 dd = make_float2(dt, dt), uu = make_float2(uf, uf);
         float2 yy = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int p = 0; p < kBulkFloats / 2; ++p) {
@@ -391,8 +384,9 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
           const float2 ab = make_float2(hw_ex2(x.x), hw_ex2(x.y));
           float2 hn;
           if (DISC == 0) {
-            const float2 w = __ffma2_rn(Bp, uu, __fmul2_rn(hp, A2[p]));
-            hn = __fmul2_rn(__ffma2_rn(ab, w, __fmul2_rn(Bp, nu)), Ik2[p]);
+            const float2 sp = __fmul2_rn(hp, A2[p]);
+            const float2 em1 = make_float2(expm1_acc(x.x, ab.x), expm1_acc(x.y, ab.y));
+            hn = __fmul2_rn(__ffma2_rn(em1, __ffma2_rn(Bp, uu, sp), sp), Ik2[p]);
           } else {
             hn = __ffma2_rn(ab, hp, __fmul2_rn(dd, __fmul2_rn(Bp, uu)));  // abar h + dt B u
           }

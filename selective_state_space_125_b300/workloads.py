@@ -12,7 +12,11 @@ not depend on the thread count):
 * u, z, B, C, D ~ N(0, 1), drawn as float32 and rounded to the workload's
   input dtype (bf16 by round-to-nearest-even, or kept as float32);
 * A_log[d, n] = log(n + 1) for every channel d (the S4D-Real initialisation,
-  A = -diag(1..N), of "State Space Models and Mamba" §1.5);
+  A = -diag(1..N), of "State Space Models and Mamba" §1.5). Since A_log is a
+  learned parameter there (A = -exp(A_log) only starts at S4D-Real), the
+  accuracy tests also draw it per (d, n), uniform on [lo, hi], from
+  ``default_rng([seed, 10, 0])``, and may set whole channels to one very
+  negative value (|A| tiny: long memory, dt A near 0);
 * delta_bias[d] = softplus^-1(sqrt(lo * hi)), the same for every d;
 * delta = softplus^-1(dt*) - delta_bias with dt* = exp(ln lo + (clip(g, -3, 3) + 3)
   / 6 * ln(hi / lo)) and g ~ N(0, 1), so that softplus(delta + bias) spans
@@ -175,12 +179,32 @@ def a_log_s4d_real(dim: int, dstate: int) -> np.ndarray:
     return np.ascontiguousarray(np.broadcast_to(row, (dim, dstate)))
 
 
+def a_log_random(dim: int, dstate: int, seed: int, lo: float, hi: float,
+                 low_channels=(), low_value: float = -12.0) -> np.ndarray:
+    """A_log[d, n] uniform on [lo, hi] (fp32), drawn from rng([seed, 10, 0]);
+    the channels listed in ``low_channels`` get ``low_value`` for every state."""
+    rng = np.random.default_rng([seed, 10, 0])
+    a = rng.uniform(lo, hi, size=(dim, dstate)).astype(np.float32)
+    for d in low_channels:
+        a[d, :] = np.float32(low_value)
+    return np.ascontiguousarray(a)
+
+
+def _a_log_for(dim, dstate, seed, a_log):
+    """``a_log`` is None (S4D-Real) or a dict of ``a_log_random`` keywords."""
+    if a_log is None:
+        return a_log_s4d_real(dim, dstate)
+    return a_log_random(dim, dstate, seed, **a_log)
+
+
 def make_scan_inputs(batch: int, dim: int, dstate: int, seqlen: int, dtype: str,
-                     seed: int, dt_range=(1e-3, 1e-1)) -> dict:
+                     seed: int, dt_range=(1e-3, 1e-1), a_log=None) -> dict:
     """Seeded scan inputs. Every array is float32 holding ``dtype``-exact values.
 
     Keys: u, delta, z (batch, seqlen, dim); B, C (batch, seqlen, dstate);
-    D, delta_bias (dim,); A_log (dim, dstate); plus 'dtype'.
+    D, delta_bias (dim,); A_log (dim, dstate); plus 'dtype'. ``a_log`` None
+    gives S4D-Real, else a dict of ``a_log_random`` keywords (lo, hi,
+    low_channels, low_value).
     """
     if dtype not in DTYPES:
         raise ValueError(f"unknown dtype {dtype!r}")
@@ -194,7 +218,7 @@ def make_scan_inputs(batch: int, dim: int, dstate: int, seqlen: int, dtype: str,
     D = _draw_normal(seed, 5, (1, dim), "f32")[0]
     return dict(u=u, delta=delta, z=z, B=B, C=C, D=D,
                 delta_bias=np.full((dim,), bias, np.float32),
-                A_log=a_log_s4d_real(dim, dstate), dtype=dtype)
+                A_log=_a_log_for(dim, dstate, seed, a_log), dtype=dtype)
 
 
 def make_config_inputs(cfg: ScanConfig, seed: int) -> dict:
@@ -203,7 +227,7 @@ def make_config_inputs(cfg: ScanConfig, seed: int) -> dict:
 
 
 def make_decode_inputs(batch: int, dim: int, dstate: int, dtype: str, seed: int,
-                       pool: int = 16, dt_range=(1e-3, 1e-1)) -> dict:
+                       pool: int = 16, dt_range=(1e-3, 1e-1), a_log=None) -> dict:
     """Seeded decode inputs: a resident state and ``pool`` distinct tokens.
 
     Keys: state0 (batch, dim, dstate) fp32; u, delta, z (pool, batch, dim);
@@ -222,7 +246,7 @@ def make_decode_inputs(batch: int, dim: int, dstate: int, dtype: str, seed: int,
     state0 = _draw_normal(seed, 6, (batch, dim, dstate), "f32")
     return dict(state0=state0, u=u, delta=delta, z=z, B=B, C=C, D=D,
                 delta_bias=np.full((dim,), bias, np.float32),
-                A_log=a_log_s4d_real(dim, dstate), dtype=dtype)
+                A_log=_a_log_for(dim, dstate, seed, a_log), dtype=dtype)
 
 
 def make_decode_config_inputs(cfg: DecodeConfig, seed: int) -> dict:
@@ -231,11 +255,11 @@ def make_decode_config_inputs(cfg: DecodeConfig, seed: int) -> dict:
 
 
 def make_bwd_inputs(batch: int, dim: int, dstate: int, seqlen: int, dtype: str,
-                    seed: int, dt_range=(1e-3, 1e-1)) -> dict:
+                    seed: int, dt_range=(1e-3, 1e-1), a_log=None) -> dict:
     """Seeded inputs of the backward scan: the scan inputs of ``make_scan_inputs``
     plus dout (batch, seqlen, dim) in ``dtype``, and h0, dlast (batch, dim, dstate)
     fp32, all N(0, 1)."""
-    inp = make_scan_inputs(batch, dim, dstate, seqlen, dtype, seed, dt_range)
+    inp = make_scan_inputs(batch, dim, dstate, seqlen, dtype, seed, dt_range, a_log)
     inp["dout"] = _draw_normal(seed, 7, (batch, seqlen, dim), dtype)
     inp["h0"] = _draw_normal(seed, 8, (batch, dim, dstate), "f32")
     inp["dlast"] = _draw_normal(seed, 9, (batch, dim, dstate), "f32")
