@@ -6,8 +6,11 @@ the selective scan of a layer (chunk load, discretisation, in-register
 recurrence, split-sequence carry when planned, fused epilogue) returning
 last_state, followed by one decode step on that state for the next token.
 
-Default workload: the Mamba-130M-shaped layer, B8 D1536 N16 L2048 bf16.
-Other workloads (--workload m1p4b|long|tiny) are available for exploration.
+Default workload: the long-sequence scan, B1 D5120 N16 L32768 bf16 (the
+largest single-GPU configuration; it takes the split-sequence carry). The
+Mamba-1.4B- and 130M-shaped layers (B16 D4096 and B8 D1536, N16 L2048 bf16) are
+timed as well and reported under "layers". Other workloads (--workload
+m1p4b|m130|tiny) can be made the headline for exploration.
 
 Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
 instead (bounded samples of the same workload on the host cores).
@@ -53,7 +56,9 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="m130", choices=sorted(SCAN_CONFIGS))
+    p.add_argument("--workload", default="long", choices=sorted(SCAN_CONFIGS))
+    p.add_argument("--no-layers", action="store_true", help="skip timing the extra layer workloads")
+    p.add_argument("--layers", default="m1p4b,m130", help="extra scan workloads timed beside the headline")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -229,6 +234,80 @@ def measure_decode(device, stream, peaks, calls=200, which=("decode", "decode128
     return out
 
 
+def scan_figures(cfg, ms, sms, peaks):
+    """Algorithmic bytes and FP32 lane-ops of one scan call of ``cfg`` and the
+    rates ``ms`` per call gives, against the HBM and FP32 peaks."""
+    B, Dm, N, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    es = 2 if cfg.dtype == "bf16" else 4
+    alg_bytes = (4 * es * B * L * Dm + 2 * N * es * B * L + Dm * N * 4 + 2 * Dm * 4
+                 + (B * Dm * N * 4 if cfg.last_state else 0))
+    alg_ops = ALG_OPS_PER_STATE_STEP * N * B * L * Dm
+    peak_tops = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e12
+    tops = alg_ops / (ms / 1e3) / 1e12
+    gbs = alg_bytes / (ms / 1e3) / 1e9
+    return dict(alg_bytes=alg_bytes, alg_ops=alg_ops, peak_tops=peak_tops, tops=tops, gbs=gbs,
+                alu_frac=tops / peak_tops, hbm_frac=gbs / peaks["hbm_gbs"])
+
+
+def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0):
+    """The scan alone on another workload (inputs resident, last_state
+    returned): CUDA events around ``calls`` graph-replayed calls that rotate
+    over input sets larger than L2 together."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    cfg = SCAN_CONFIGS[name]
+    B, Dm, N, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    inp = make_config_inputs(cfg, seed=seed)
+    dev_x = lambda a: torch.from_numpy(bf16_bits(a).view(np.int16)).to(device).view(torch.bfloat16)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    base = {k: dev_x(inp[k]) for k in ("u", "delta", "z", "B", "C")}
+    A_log, Dv, bias = f32(inp["A_log"]), f32(inp["D"]), f32(inp["delta_bias"])
+    del inp
+    set_bytes = sum(t.numel() * t.element_size() for t in base.values()) + B * L * Dm * 2
+    nsets = max(2, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    sets = []
+    for i in range(nsets):
+        st = {k: (v if i == 0 else v.clone()) for k, v in base.items()}
+        st["out"] = torch.empty((B, L, Dm), dtype=torch.bfloat16, device=device)
+        st["last"] = torch.empty((B, Dm, N), dtype=torch.float32, device=device)
+        sets.append(st)
+    chosen, launches = binding.mamba_selective_scan_plan(B, Dm, N, L, cfg.dtype)
+
+    def scan(st):
+        binding.mamba_selective_scan_fwd(st["u"], st["delta"], A_log, st["B"], st["C"], Dv, st["z"], bias,
+                                         st["out"], st["last"])
+    for i in range(3):
+        scan(sets[i % nsets])
+    torch.cuda.synchronize(device)
+    graphs = []
+    for st in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            scan(st)
+        graphs.append(g)
+    for i in range(nsets):
+        graphs[i].replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(calls):
+        graphs[i % nsets].replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    assert binding.mamba_device_status() == 0, "a kernel reported a timeout"
+    ms = e0.elapsed_time(e1) / calls
+    f = scan_figures(cfg, ms, sms, peaks)
+    del sets, graphs, base
+    torch.cuda.empty_cache()
+    return {"workload": cfg.description, "kernel_ms": ms, "channel_steps_per_s": B * Dm * L / (ms / 1e3),
+            "hbm": {"achieved": f["gbs"], "unit": "GB/s", "frac": f["hbm_frac"], "bytes_per_call": f["alg_bytes"]},
+            "alu": {"achieved": f["tops"], "unit": "T FP32 lane-op/s", "frac": f["alu_frac"],
+                    "ops_per_call": f["alg_ops"]},
+            "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
+                     "launches": launches},
+            "calls": calls, "l2": f"{nsets} rotating input sets of {set_bytes / 2**20:.0f} MiB"}
+
+
 # ------------------------------------------------------------- our arm
 def run_ours(args, rank, world, device):
     import torch
@@ -382,12 +461,9 @@ def run_ours(args, rank, world, device):
     peaks = read_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     scan_avg_ms = float(np.mean(scan_ms))
-    alg_bytes = (4 * es * B * L * Dm + 2 * N * es * B * L + Dm * N * 4 + 2 * Dm * 4
-                 + (B * Dm * N * 4 if cfg.last_state else 0))
-    alg_ops = ALG_OPS_PER_STATE_STEP * N * B * L * Dm
-    achieved_tops = alg_ops / (scan_avg_ms / 1e3) / 1e12
-    peak_tops = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e12
-    achieved_gbs = alg_bytes / (scan_avg_ms / 1e3) / 1e9
+    fig = scan_figures(cfg, scan_avg_ms, sms, peaks)
+    alg_bytes, alg_ops, peak_tops = fig["alg_bytes"], fig["alg_ops"], fig["peak_tops"]
+    achieved_tops, achieved_gbs = fig["tops"], fig["gbs"]
     clocks = sampler.summary(t_wall0, t_wall1)
     traffic, traffic_note = None, "no ncu summary for this workload and plan"
     if os.path.exists(TRAFFIC_FILE):
@@ -478,7 +554,7 @@ def run_ours(args, rank, world, device):
     result = {
         "metric": METRIC, "value": value, "unit": "channel-steps/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy, see DESIGN.md)",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded numpy draws of the workload's shapes and distributions)",
         "config": {"workload": cfg.description, "batch": B, "d_inner": Dm, "d_state": N, "seqlen": L,
                    "input_dtype": cfg.dtype, "state_dtype": "f32",
                    "step": "scan(L tokens, last_state) + 1 decode step", "channel_steps_per_step": chsteps,
@@ -509,6 +585,11 @@ def run_ours(args, rank, world, device):
         result["scan_conv1d_fused"] = conv
     if bwd is not None:
         result["scan_bwd"] = bwd
+    if not args.no_layers:
+        del sets
+        torch.cuda.empty_cache()
+        result["layers"] = {name: measure_layer(name, device, stream, peaks, sms)
+                            for name in args.layers.split(",") if name and name != args.workload}
     return result
 
 
@@ -542,10 +623,14 @@ def oracle_sample_rate(cfg, inp, seconds, threads):
 
 
 def cpu_baseline(args, cfg):
+    """The fp64 oracle on all host cores (the value) and on one core, each on a
+    bounded sample of the workload."""
     threads = os.cpu_count() or 1
     inp = make_config_inputs(cfg, seed=args.seed)
     rate, sample = oracle_sample_rate(cfg, inp, args.cpu_seconds, threads)
-    return {"value": rate, "unit": "channel-steps/s", "cores": threads, "kind": "oracle", "sample": sample}
+    rate1, sample1 = oracle_sample_rate(cfg, inp, args.cpu_seconds / 2, 1)
+    return {"value": rate, "unit": "channel-steps/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "single_core": {"value": rate1, "unit": "channel-steps/s", "cores": 1, "sample": sample1}}
 
 
 def run_reference(args, rank, world):
