@@ -30,13 +30,15 @@
 //     is s <- s + (Abar - 1)(s + B u), and y = sum (C / A) s, all on packed
 //     f32x2 FMUL/FFMA pairs of states, with Abar by MUFU ex2 and Abar - 1 =
 //     ex2 - 1. Where dt |A| is small, ex2 - 1 loses the input term to
-//     cancellation (relative error near 2^-23 / |dt A|), so before each chunk
-//     the CTA checks its delta tile against a per-channel bound (the delta
-//     at which dt |A| = 2^-14 for the channel's smallest |A|): if some step
-//     of some channel falls below it, the whole chunk takes Abar - 1 from a
-//     short series instead (expm1_acc). The check rides on the chunk's
-//     barrier (__syncthreads_or), so the unrolled step loop carries no
-//     branch. |A| is floored at 1e-20, where Abar and (Abar - 1) / A equal
+//     cancellation (relative error near 2^-23 / |dt A|). So every chunk runs
+//     optimistically: each thread saves its state to shared memory, runs the
+//     chunk with ex2 - 1 keeping the smallest dt it met, and compares that
+//     with its channel's bound (dt |A| = 2^-14 for the channel's smallest
+//     |A|). If a lane of the warp fell below, the warp restores its state and
+//     runs the chunk again with Abar - 1 from a short series (expm1_acc),
+//     overwriting the chunk's outputs; its inputs are still staged. The common
+//     path pays one min per step group and four 16-byte stores per chunk, and its
+//     unrolled step loop carries no branch. |A| is floored at 1e-20, where Abar and (Abar - 1) / A equal
 //     their A -> 0 limits (1 and dt) in fp32 ("State Space Models and Mamba"
 //     §2, the zero-order hold's limit). fp32 inputs use the precise path on
 //     the unscaled state with expm1f, so that (Abar - 1) / A keeps full
@@ -85,11 +87,13 @@ struct ScanGeom {
   static constexpr size_t kBCTile = scan_a128(size_t(kChunk) * kNP * kES);
   static constexpr size_t kStage = kUTile + 2 * kXTile + 2 * kBCTile;
   static constexpr size_t kBC32 = scan_a128(size_t(kChunk) * 2 * kNP * 4);  // [t][B | C][NP] fp32, x2 buffers
-  static constexpr size_t kChan = scan_a128(size_t(kCB) * 3 * 4);           // bias, D, delta bound per channel
+  static constexpr size_t kChan = scan_a128(size_t(kCB) * 2 * 4);           // bias, D per channel
+  static constexpr size_t kSave = scan_a128(size_t(kScanThreads) * NPL * 4);  // each thread's state at a chunk start
   static constexpr size_t kBar = 128;
   static constexpr size_t kOffBC32 = kStages * kStage;
   static constexpr size_t kOffChan = kOffBC32 + 2 * kBC32;
-  static constexpr size_t kOffBar = kOffChan + kChan;
+  static constexpr size_t kOffSave = kOffChan + kChan;
+  static constexpr size_t kOffBar = kOffSave + kSave;
   static constexpr size_t kSmem = kOffBar + kBar + 128;  // + alignment slack of the dynamic base
   static_assert(kChunk % LPC == 0, "a chunk holds whole step groups");
   static_assert(kSmem <= 227 * 1024, "scan variant exceeds the shared memory of one CTA");
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_dyn) + 127) & ~uintptr_t(127));
   float* chan_bias = reinterpret_cast<float*>(smem + G::kOffChan);
   float* chan_D = chan_bias + CB;
-  float* chan_dmin = chan_D + CB;  // delta at or above which a step of the channel may take the fast em1
+  float4* save = reinterpret_cast<float4*>(smem + G::kOffSave);  // [NPL / 4][threads]
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem + G::kOffBar);
 
   // Stage s: u tile (kURows rows; with CONV its first kConvHalo rows are the
@@ -378,16 +382,12 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   }
   const float bias = chan_bias[c];
   const float Dd = chan_D[c];
+  // dt below which a step of my channel needs the accurate Abar - 1
+  float thr = 0.0f;
   if constexpr (SCALED) {
-    // The channel's delta bound: dt = softplus(delta + bias) >= kFastMinDtA / min|A|
-    // exactly when delta >= softplus^-1(kFastMinDtA / min|A|) - bias.
 #pragma unroll
     for (int o = 1; o < LPC; o <<= 1) minA = fminf(minA, __shfl_xor_sync(0xffffffffu, minA, o));
-    if (q == 0) {
-      const float dtb = kFastMinDtA / minA;
-      chan_dmin[c] = (dtb > 20.0f ? dtb : logf(expm1f(dtb))) - bias;
-    }
-    __syncthreads();
+    thr = kFastMinDtA / minA;
   }
   // Conv taps aligned to the u tile: tap j multiplies row tm + j (input step
   // t - kConvHalo + j), so a width-W kernel fills taps kConvHalo + 1 - W .. kConvHalo.
@@ -409,7 +409,10 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   double dsum_d = 0.0;  // AGG: the same in fp64 (precise path)
 
   // The steps of one staged chunk (see the loop below).
-  auto run_chunk = [&]<bool HZ, bool ACC>(int s, int kc, int t0, int tv) {
+  // Returns (fast path) whether a lane of the warp met a step with dt < thr
+  // (steps past the end count too: a ragged last chunk may be rerun for nothing).
+  auto run_chunk = [&]<bool HZ, bool ACC>(int s, int kc, int t0, int tv) -> bool {
+    [[maybe_unused]] float dtmin = 3.0e38f;
     const Tin* su = xu(s) + c;
     const Tin* sd = xd(s) + c;
     const Tin* sz = xz(s) + c;
@@ -432,6 +435,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       const bool live = tm < tv;
       dtv = live ? dt : 0.0f;
       uv = live ? um : 0.0f;
+      if constexpr (SCALED && !ACC) dtmin = fminf(dtmin, dt);
     };
     float dt_nx, u_nx;
     lane_dtu(q, dt_nx, u_nx);
@@ -478,6 +482,8 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       if (HZ) y *= PRECISE ? silu_precise(z_pv) : silu_fast(z_pv);
       if (dvalid && CH - LPC + q < tv) E::store(gout + (size_t)(CH - LPC) * Dm, y);
     }
+    if constexpr (SCALED && !ACC) return __any_sync(0xffffffffu, dtmin < thr);
+    return false;
   };
 
   for (int k = 0; k < nchunks; ++k) {
@@ -512,32 +518,6 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
         xd(s)[i] = in ? gdl[off] : Tin(0.0f);
         if (has_z) xz(s)[i] = in ? gz[off] : Tin(0.0f);
       }
-      if constexpr (SCALED) __syncthreads();  // the delta check below reads other threads' rows
-    }
-    // Whether some channel of the CTA has a step in this chunk with dt |A|
-    // below kFastMinDtA: the CB/2 channel pairs x CH rows of the delta tile
-    // are split over the threads, RPT rows of one pair each (packed bf16
-    // pairs, a min tree); each thread compares its rows' smallest delta with
-    // its pair's bounds, and the chunk's barrier below ORs the answers over
-    // the CTA. The loads are issued here so that they overlap the widening.
-    bool slow = false;
-    if constexpr (SCALED) {
-      constexpr int PAIRS = CB / 2;
-      constexpr int RPT = (CH * PAIRS + kScanThreads - 1) / kScanThreads;  // rows per thread
-      const int p = tid % PAIRS, r0 = (tid / PAIRS) * RPT;
-      const __nv_bfloat162* col = reinterpret_cast<const __nv_bfloat162*>(xd(s)) + p;
-      const __nv_bfloat162 inf2 = __bfloat162bfloat162(__ushort_as_bfloat16(0x7F80u));
-      __nv_bfloat162 m[RPT];
-#pragma unroll
-      for (int i = 0; i < RPT; ++i) m[i] = (r0 + i < tv) ? col[(r0 + i) * PAIRS] : inf2;
-#pragma unroll
-      for (int w = 1; w < RPT; w *= 2)
-#pragma unroll
-        for (int i = 0; i + w < RPT; i += 2 * w) m[i] = __hmin2(m[i], m[i + w]);
-      if (r0 < tv) {
-        const float2 mf = __bfloat1622float2(m[0]);
-        slow = mf.x < chan_dmin[2 * p] || mf.y < chan_dmin[2 * p + 1];
-      }
     }
     // B / C rows widened to fp32 once for every channel of the CTA (zero beyond N).
     float* bck = bc32(k);
@@ -557,11 +537,7 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
       bck[t * 2 * NP + n] = bv;
       bck[t * 2 * NP + NP + n] = cv;
     }
-    if constexpr (SCALED) {
-      slow = __syncthreads_or(slow);  // chunk k staged; every thread is past chunk k-1
-    } else {
-      __syncthreads();  // chunk k staged; every thread is past chunk k-1
-    }
+    __syncthreads();  // chunk k staged; every thread is past chunk k-1
     if (use_tma && tid == 0 && k >= 1 && issued < nchunks) {
       fence_proxy_async_smem();  // chunk k-1's stage was read through the generic proxy
       issue(issued);
@@ -574,16 +550,30 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     // is (Abar = 1, no input), and store nothing. The loop is branch-free and
     // fully unrolled so that the compiler can overlap a group's recurrence
     // with the next group's softplus and the previous group's epilogue.
-    if (slow) {
-      if (has_z)
-        run_chunk.template operator()<true, true>(s, k, t0, tv);
-      else
-        run_chunk.template operator()<false, true>(s, k, t0, tv);
+    if constexpr (SCALED) {
+      // optimistic fast pass; the warp reruns the chunk accurately if it met a small dt |A|
+#pragma unroll
+      for (int j = 0; j < NH; j += 2) save[(j / 2) * kScanThreads + tid] = make_float4(st[j].x, st[j].y, st[j + 1].x, st[j + 1].y);
+      const float dsum0 = dsum;
+      const bool redo = has_z ? run_chunk.template operator()<true, false>(s, k, t0, tv)
+                              : run_chunk.template operator()<false, false>(s, k, t0, tv);
+      if (redo) {
+#pragma unroll
+        for (int j = 0; j < NH; j += 2) {
+          const float4 v = save[(j / 2) * kScanThreads + tid];
+          st[j] = make_float2(v.x, v.y);
+          st[j + 1] = make_float2(v.z, v.w);
+        }
+        dsum = dsum0;
+        if (has_z)
+          run_chunk.template operator()<true, true>(s, k, t0, tv);
+        else
+          run_chunk.template operator()<false, true>(s, k, t0, tv);
+      }
+    } else if (has_z) {
+      run_chunk.template operator()<true, false>(s, k, t0, tv);
     } else {
-      if (has_z)
-        run_chunk.template operator()<true, false>(s, k, t0, tv);
-      else
-        run_chunk.template operator()<false, false>(s, k, t0, tv);
+      run_chunk.template operator()<false, false>(s, k, t0, tv);
     }
   }
 
