@@ -249,10 +249,11 @@ def scan_figures(cfg, ms, sms, peaks):
                 alu_frac=tops / peak_tops, hbm_frac=gbs / peaks["hbm_gbs"])
 
 
-def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0):
+def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0, time_lanes=0):
     """The scan alone on another workload (inputs resident, last_state
     returned): CUDA events around ``calls`` graph-replayed calls that rotate
-    over input sets larger than L2 together."""
+    over input sets larger than L2 together. ``time_lanes`` > 1 times the
+    time-parallel chunk scan in place of the automatic plan."""
     import torch
     from selective_state_space_125_b300 import binding
     cfg = SCAN_CONFIGS[name]
@@ -271,11 +272,12 @@ def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0):
         st["out"] = torch.empty((B, L, Dm), dtype=torch.bfloat16, device=device)
         st["last"] = torch.empty((B, Dm, N), dtype=torch.float32, device=device)
         sets.append(st)
-    chosen, launches = binding.mamba_selective_scan_plan(B, Dm, N, L, cfg.dtype)
+    plan = binding.ScanPlan(0, 0, 0, 0, time_lanes) if time_lanes > 1 else None
+    chosen, launches = binding.mamba_selective_scan_plan(B, Dm, N, L, cfg.dtype, plan)
 
     def scan(st):
         binding.mamba_selective_scan_fwd(st["u"], st["delta"], A_log, st["B"], st["C"], Dv, st["z"], bias,
-                                         st["out"], st["last"])
+                                         st["out"], st["last"], plan=plan)
     for i in range(3):
         scan(sets[i % nsets])
     torch.cuda.synchronize(device)
@@ -304,7 +306,7 @@ def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0):
             "alu": {"achieved": f["tops"], "unit": "T FP32 lane-op/s", "frac": f["alu_frac"],
                     "ops_per_call": f["alg_ops"]},
             "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
-                     "launches": launches},
+                     "time_lanes": chosen.time_lanes, "launches": launches},
             "calls": calls, "l2": f"{nsets} rotating input sets of {set_bytes / 2**20:.0f} MiB"}
 
 
@@ -590,6 +592,11 @@ def run_ours(args, rank, world, device):
         torch.cuda.empty_cache()
         result["layers"] = {name: measure_layer(name, device, stream, peaks, sms)
                             for name in args.layers.split(",") if name and name != args.workload}
+        # The time-parallel chunk scan (plan knob time_lanes) on the 130M-shaped
+        # layer, whose 12,288 channels leave the sequential plan short of warps.
+        for tl in (2, 4):
+            result["layers"][f"m130_time_lanes_{tl}"] = measure_layer("m130", device, stream, peaks, sms,
+                                                                     time_lanes=tl)
     return result
 
 

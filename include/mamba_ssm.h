@@ -142,13 +142,27 @@ typedef enum {
  *                       run in parallel, joined by the two-pass carry (1 = off);
  *   use_tma           : 0 auto, 1 require the TMA tile loader (error if the
  *                       layout does not allow it), 2 force plain loads;
- *   discretization    : a mamba_discretization_t value.
+ *   discretization    : a mamba_discretization_t value;
+ *   time_lanes        : 0 or 1: each lane walks time sequentially (the default).
+ *                       2 or 4: the time-parallel chunk scan: that many lanes
+ *                       share a channel, each holding all its states and
+ *                       scanning its part of every 16-step chunk; the parts
+ *                       are joined by a warp-shuffle scan under the operator
+ *                       (a, b) o (a', b') = (a a', a' b + b') and each lane
+ *                       fixes its readouts up with the exact state entering
+ *                       its part ("State Space Models and Mamba" §4, parallel
+ *                       scan). Needs N <= 16, zero-order hold, one segment
+ *                       (segments 0 or 1) and lanes_per_channel 0 or 1, and
+ *                       is not available with the fused conv1d
+ *                       (MAMBA_ERR_UNSUPPORTED / MAMBA_ERR_INVALID_ARG).
+ *                       Automatic plans never choose it.
  */
 typedef struct {
     int lanes_per_channel;
     int segments;
     int use_tma;
     int discretization;
+    int time_lanes;
 } mamba_scan_plan_t;
 
 /*

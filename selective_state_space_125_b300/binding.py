@@ -36,9 +36,11 @@ _lib = None
 
 
 class ScanPlan(ctypes.Structure):
-    """mamba_scan_plan_t: 0 in a field means automatic (ZOH for discretization)."""
+    """mamba_scan_plan_t: 0 in a field means automatic (ZOH for discretization,
+    sequential time for time_lanes)."""
     _fields_ = [("lanes_per_channel", ctypes.c_int), ("segments", ctypes.c_int),
-                ("use_tma", ctypes.c_int), ("discretization", ctypes.c_int)]
+                ("use_tma", ctypes.c_int), ("discretization", ctypes.c_int),
+                ("time_lanes", ctypes.c_int)]
 
 
 class MambaError(RuntimeError):

@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmamba_ssm_b300.so")
 SOURCES = ["api.cu", "scan_f32.cu", "scan_bf16.cu", "scan_f32_simple.cu", "scan_bf16_simple.cu",
            "scan_f32_conv.cu", "scan_bf16_conv.cu", "state_update.cu", "scan_bwd.cu", "scan_bwd_full.cu",
-           "scan_bwd_agg.cu"]
+           "scan_bwd_agg.cu", "scan_tp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++20", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
