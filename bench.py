@@ -57,12 +57,15 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="long", choices=sorted(SCAN_CONFIGS))
+    p.add_argument("--seqlen", type=int, default=0,
+                   help="override the workload's sequence length (smaller profiling cases of the same kernel)")
     p.add_argument("--no-layers", action="store_true", help="skip timing the extra layer workloads")
     p.add_argument("--layers", default="m1p4b,m130", help="extra scan workloads timed beside the headline")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=100)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
+    p.add_argument("--cpu-threads", type=int, default=0, help="--impl reference: host threads (0: all cores)")
     p.add_argument("--lanes", type=int, default=0, help="plan override: lanes per channel")
     p.add_argument("--segments", type=int, default=0, help="plan override: time segments")
     p.add_argument("--no-decode", action="store_true", help="skip the full-size decode measurement")
@@ -310,12 +313,60 @@ def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0, time_lanes
             "calls": calls, "l2": f"{nsets} rotating input sets of {set_bytes / 2**20:.0f} MiB"}
 
 
+def measure_bwd_layer(name, device, stream, peaks, sms, calls=20, seed=0):
+    """The backward scan on a layer workload (random dout; the call's memsets
+    included): ms per call, against the FP32 peak at the backward's lane-op count."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    cfg = SCAN_CONFIGS[name]
+    B, Dm, N, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
+    inp = make_config_inputs(cfg, seed=seed)
+    dev_x = lambda a: torch.from_numpy(bf16_bits(a).view(np.int16)).to(device).view(torch.bfloat16)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    t = {k: dev_x(inp[k]) for k in ("u", "delta", "z", "B", "C")}
+    A_log, Dv, bias = f32(inp["A_log"]), f32(inp["D"]), f32(inp["delta_bias"])
+    del inp
+    dout = torch.randn((B, L, Dm), device=device, generator=torch.Generator(device).manual_seed(11)).to(torch.bfloat16)
+
+    def call():
+        return binding.mamba_selective_scan_bwd(t["u"], t["delta"], A_log, t["B"], t["C"], dout, D=Dv, z=t["z"],
+                                                delta_bias=bias)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(calls):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    assert binding.mamba_device_status() == 0, "a kernel reported a timeout"
+    ms = e0.elapsed_time(e1) / calls
+    ops = ALG_BWD_OPS_PER_STATE_STEP * N * B * L * Dm
+    peak = FP32_LANES_PER_SM * sms * peaks["sm_max_mhz"] * 1e6 / 1e12
+    del t, dout
+    torch.cuda.empty_cache()
+    return {"workload": cfg.description + ", backward", "ms_per_call": ms,
+            "channel_steps_per_s": B * L * Dm / (ms / 1e3), "achieved": ops / (ms / 1e3) / 1e12,
+            "unit": "T FP32 lane-op/s", "frac": ops / (ms / 1e3) / 1e12 / peak, "calls": calls}
+
+
 # ------------------------------------------------------------- our arm
+def workload_config(args):
+    """The headline workload, with its sequence length overridden by --seqlen."""
+    import dataclasses
+    cfg = SCAN_CONFIGS[args.workload]
+    if args.seqlen > 0:
+        cfg = dataclasses.replace(cfg, seqlen=args.seqlen,
+                                  description=f"{cfg.description} with L = {args.seqlen}")
+    return cfg
+
+
 def run_ours(args, rank, world, device):
     import torch
     from selective_state_space_125_b300 import binding
 
-    cfg = SCAN_CONFIGS[args.workload]
+    cfg = workload_config(args)
     B, Dm, N, L = cfg.batch, cfg.dim, cfg.dstate, cfg.seqlen
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     es = 2 if cfg.dtype == "bf16" else 4
@@ -470,7 +521,7 @@ def run_ours(args, rank, world, device):
     traffic, traffic_note = None, "no ncu summary for this workload and plan"
     if os.path.exists(TRAFFIC_FILE):
         with open(TRAFFIC_FILE) as f:
-            tr = json.load(f).get(args.workload)
+            tr = json.load(f).get(args.workload) if args.seqlen == 0 else None
         if tr and tr.get("plan") == [chosen.lanes_per_channel, chosen.segments] and \
                 tr.get("kernel_source_sha") == kernel_source_sha():
             traffic, traffic_note = tr.get("dram_bytes_per_call"), tr.get("source")
@@ -597,6 +648,7 @@ def run_ours(args, rank, world, device):
         for tl in (2, 4):
             result["layers"][f"m130_time_lanes_{tl}"] = measure_layer("m130", device, stream, peaks, sms,
                                                                      time_lanes=tl)
+        result["layers"]["m130_bwd"] = measure_bwd_layer("m130", device, stream, peaks, sms)
     return result
 
 
@@ -643,11 +695,11 @@ def cpu_baseline(args, cfg):
 def run_reference(args, rank, world):
     """--impl reference: the fp64 oracle on host cores, K timed steps of bounded samples."""
     import oracle
-    cfg = SCAN_CONFIGS[args.workload]
-    threads = os.cpu_count() or 1
+    cfg = workload_config(args)
+    threads = args.cpu_threads if args.cpu_threads > 0 else (os.cpu_count() or 1)
     inp = make_config_inputs(cfg, seed=args.seed)
     L, Dm = cfg.seqlen, cfg.dim
-    budget = 120.0 / max(1, args.steps + args.warmup)   # seconds per step
+    budget = min(args.cpu_seconds, 120.0 / max(1, args.steps + args.warmup))   # seconds per step
     rate, _ = oracle_sample_rate(cfg, inp, min(2.0, budget), threads)
     k = max(1, min(Dm, int(budget * rate / L)))
     sl = slice(0, k)
@@ -706,7 +758,7 @@ def main():
     result = run_ours(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            result["cpu_baseline"] = cpu_baseline(args, SCAN_CONFIGS[args.workload])
+            result["cpu_baseline"] = cpu_baseline(args, workload_config(args))
         print(json.dumps(result), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

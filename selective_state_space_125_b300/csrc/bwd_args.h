@@ -9,10 +9,9 @@ namespace mamba {
 constexpr int kBwdThreads = 128;  // threads per CTA of the backward kernel
 constexpr int kBwdChunk = 16;     // time steps per chunk (checkpoint interval)
 constexpr int kBwdMaxSegments = 64;
-// Smallest |dt A| at which the bf16 backward forms abar - 1 as ex2 - 1 and
-// dA_log as the difference of its two first-order-equal terms (relative
-// error of each step's dA_log term below 2^-23 / (|dt A| / 2) = 2^-10 there).
-constexpr float kBwdFastMinDtA = 2.44140625e-04f;  // 2^-12
+// Smallest |dt A| at which the bf16 backward forms abar - 1 as ex2 - 1
+// (relative error below 2^-23 / |dt A| = 2^-9 there), as the forward does.
+constexpr float kBwdFastMinDtA = 6.103515625e-05f;  // 2^-14
 
 // Passes of the backward kernel.
 constexpr int kBwdFull = 0;    // the gradients over one time segment

@@ -32,16 +32,17 @@
 // Math: bf16 inputs use MUFU ex2/rcp and keep the scaled state s = A h during
 // the recomputation (s_t = s_{t-1} + (abar - 1)(s_{t-1} + B u), so A h_{t-1} is
 // read directly); fp32 inputs use expm1f and the unscaled h, as the forward
-// does. Where dt |A| is small, abar - 1 formed as ex2 - 1, and the dA_log
-// term dt abar lambda v - q lambda B u (whose two parts agree to first order in
-// dt A), lose their leading digits. So, as in the forward, a step whose warp
-// holds a state with dt |A| < 2^-12 takes the accurate form instead (a
-// warp-uniform branch; fp32 inputs always do): abar - 1 from expm1_acc, and
+// does. dA_log is accumulated as
 //   dA_log = A sum_t lambda_t dt_t (abar h_{t-1} + dt_t phi'(dt A) B u),
-// phi(x) = (e^x - 1) / x, phi'(x) = (x e^x - e^x + 1) / x^2 from its series below
-// |x| = 1/8 (the A factor is taken out so that |A| below the kernels' 1e-20
-// floor still gives the exact dA_log). dA_log sums the fast and accurate
-// parts.
+// phi(x) = (e^x - 1) / x, phi'(x) = (x e^x - e^x + 1) / x^2 taken from its
+// series below |x| = 1/8 and its closed form above. (The equivalent difference
+// dt abar lambda v - q lambda B u cancels to first order in dt A: an error of
+// the hardware exp(dt A) of size e becomes a relative error near 2 e / (dt A)^2
+// of the difference.) The A factor is taken out so that |A| below the
+// kernels' 1e-20 floor still gives the exact dA_log. abar - 1 (for q and the
+// recomputation) is ex2 - 1 unless a state of the warp has dt |A| < 2^-14 at
+// that step, when the step takes expm1_acc (a warp-uniform branch; fp32
+// inputs use expm1f throughout).
 //
 // Time segments (for small batch x channels over long sequences): the
 // sequence is cut into S segments of whole chunks, one CTA per (channel
@@ -226,21 +227,32 @@ __device__ __forceinline__ float dphi_acc(float xl, float e, float em1, float ix
   return (fabsf(x) < 0.125f) ? ser : (e - em1 * ix) * ix;
 }
 
+// dphi_acc for a packed pair: both branches in f32x2 arithmetic, one select per element.
+__device__ __forceinline__ float2 dphi_acc2(float2 xl, float2 e, float2 em1, float2 ix) {
+  const float2 x = __fmul2_rn(xl, make_float2(kLn2, kLn2));
+  const float2 ser = __ffma2_rn(x, __ffma2_rn(x, __ffma2_rn(x, make_float2(1.0f / 30.0f, 1.0f / 30.0f),
+                                                          make_float2(1.0f / 8.0f, 1.0f / 8.0f)),
+                                            make_float2(1.0f / 3.0f, 1.0f / 3.0f)),
+                                make_float2(0.5f, 0.5f));
+  const float2 closed = __fmul2_rn(__ffma2_rn(make_float2(-em1.x, -em1.y), ix, e), ix);
+  return make_float2(fabsf(x.x) < 0.125f ? ser.x : closed.x, fabsf(x.y) < 0.125f ? ser.y : closed.y);
+}
+
 // ---------------------------------------------------- adjoint step (4 states)
 // Given s_t (sn), s_{t-1} (sp) and lambda_{t+1} abar_{t+1} (carry): updates
 // carry to abar_t lambda_t, adds the dA_log terms, writes the dB partials to
 // v[0..3] and the dC partials to v[4..7], and returns the sums over the 4
 // states of the du, dt and y terms.
-// ACC = false: abar - 1 = ex2 - 1 and the dA_log terms in dApos - dAneg;
-// ACC = true: expm1_acc, and the dA_log terms (without their A factor) in G.
+// ACC selects abar - 1: ex2 - 1 (false) or expm1_acc (true). The dA_log terms
+// (without their A factor) go to G.
 template <int DISC, bool ACC>
 __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, float4 C4, float dt, float uu, float dy,
-                                              float2 (&carry)[2], float2 (&dApos)[2], float2 (&dAneg)[2],
-                                              float2 (&G)[2], const float2 (&Al)[2], const float2 (&Ik)[2],
-                                              float (&v)[8], float& dus, float& ddt, float& ys) {
+                                              float2 (&carry)[2], float2 (&G)[2], const float2 (&Al)[2],
+                                              const float2 (&Ik)[2], float (&v)[8], float& dus, float& ddt,
+                                              float& ys) {
   const float2 dd = dup2(dt), u2 = dup2(uu), yy = dup2(dy);
   float2 sdus = make_float2(0.f, 0.f), sddt = sdus, sys = sdus;
-  [[maybe_unused]] const float rdt = ACC ? hw_rcp(dt) : 0.0f;  // 1 / dt (dt = 0 only where |x| < 1/8)
+  [[maybe_unused]] const float rdt = DISC == 0 ? hw_rcp(dt) : 0.0f;  // 1 / dt (dt = 0 only where |x| < 1/8)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
@@ -262,16 +274,11 @@ __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, f
       const float2 q = __fmul2_rn(em1, Ik[h]);                 // (abar - 1) / A
       r = __fmul2_rn(lam, q);
       m = __fmul2_rn(al, __fadd2_rn(spp, Bu));                  // abar lambda (A h_{t-1} + B u)
-      if constexpr (ACC) {
-        const float2 ix = __fmul2_rn(Ik[h], dup2(rdt));         // 1 / (dt A)
-        const float2 dp = make_float2(dphi_acc(x.x, ab.x, em1.x, ix.x), dphi_acc(x.y, ab.y, em1.y, ix.y));
-        const float2 hp = __fmul2_rn(spp, Ik[h]);               // h_{t-1}
-        const float2 inner = __ffma2_rn(al, hp, __fmul2_rn(__fmul2_rn(dd, dp), __fmul2_rn(lam, Bu)));
-        G[h] = __ffma2_rn(dd, inner, G[h]);                     // dt (abar h + dt phi' B u) lambda
-      } else {
-        dApos[h] = __ffma2_rn(dd, m, dApos[h]);                 // + dt abar lambda v
-        dAneg[h] = __ffma2_rn(r, Bu, dAneg[h]);                 // - q lambda B u
-      }
+      const float2 ix = __fmul2_rn(Ik[h], dup2(rdt));           // 1 / (dt A)
+      const float2 dp = dphi_acc2(x, ab, em1, ix);
+      const float2 hp = __fmul2_rn(spp, Ik[h]);                 // h_{t-1}
+      const float2 inner = __ffma2_rn(al, hp, __fmul2_rn(__fmul2_rn(dd, dp), __fmul2_rn(lam, Bu)));
+      G[h] = __ffma2_rn(dd, inner, G[h]);                       // dt (abar h + dt phi' B u) lambda
     } else {
       r = __fmul2_rn(lam, dd);
       m = __ffma2_rn(al, spp, __fmul2_rn(lam, Bu));             // lambda (abar A h_{t-1} + B u)
@@ -511,7 +518,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 
   // --------------------------------------------------- phase 2: adjoint
   float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs (dAl: without the A factor)
-  float2 carry2[2], dApos[2], dAneg[2], G2[2];        // bf16 inputs (G2: accurate terms, without A)
+  float2 carry2[2], G2[2];                            // bf16 inputs (G2: dA_log terms without the A factor)
   {
     float4 g = (MODE == kBwdFull && cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
     if constexpr (MODE == kBwdFull) {
@@ -526,7 +533,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
     carry2[0] = lo2(g);
     carry2[1] = hi2(g);  // (kBwdAdjAgg runs on the scalar carry for either input type)
-    dApos[0] = dApos[1] = dAneg[0] = dAneg[1] = G2[0] = G2[1] = make_float2(0.f, 0.f);
+    G2[0] = G2[1] = make_float2(0.f, 0.f);
   }
   float dD_acc = 0.0f, dbias_acc = 0.0f;  // channel d0 + tid % CB
   XCopy4 xq;
@@ -629,11 +636,9 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
           if constexpr (PRECISE)
             adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
           else if (__all_sync(0xffffffffu, tc.x >= thr))
-            adj_step_fast<DISC, false>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, G2, Al2, Ik2, v, dus,
-                                       ddt, ys);
+            adj_step_fast<DISC, false>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, G2, Al2, Ik2, v, dus, ddt, ys);
           else
-            adj_step_fast<DISC, true>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, dApos, dAneg, G2, Al2, Ik2, v, dus,
-                                      ddt, ys);
+            adj_step_fast<DISC, true>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, G2, Al2, Ik2, v, dus, ddt, ys);
           sn = sp;
         }
 #pragma unroll
@@ -710,8 +715,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       dA4 = make_float4(Atrue[0] * dAl[0], Atrue[1] * dAl[1], Atrue[2] * dAl[2], Atrue[3] * dAl[3]);
       g4 = make_float4(carry[0], carry[1], carry[2], carry[3]);
     } else {
-      dA4 = make_float4(fmaf(Atrue[0], G2[0].x, dApos[0].x - dAneg[0].x), fmaf(Atrue[1], G2[0].y, dApos[0].y - dAneg[0].y),
-                        fmaf(Atrue[2], G2[1].x, dApos[1].x - dAneg[1].x), fmaf(Atrue[3], G2[1].y, dApos[1].y - dAneg[1].y));
+      dA4 = make_float4(Atrue[0] * G2[0].x, Atrue[1] * G2[0].y, Atrue[2] * G2[1].x, Atrue[3] * G2[1].y);
       g4 = make_float4(carry2[0].x, carry2[0].y, carry2[1].x, carry2[1].y);
     }
     atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), dA4);

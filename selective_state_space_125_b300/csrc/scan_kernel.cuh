@@ -344,10 +344,10 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
 
   // Per-thread constants for my NPL states:
   //  fast:    Ak = A * log2(e) (exponent for ex2), Ik = 1 / A;
-  //  precise: Ak = A,                              Ik = 1 / A (0 if A == 0).
-  // Initial state: h0 (or 0), then the composed aggregates of earlier segments.
+  //  precise: Ak = A,                              Ik = 1 / A.
   // A = -exp(A_log) with |A| >= kMinAbsA.
   float2 Ak[NH], Ik[NH], st[NH];
+  float Av[NPL], hin[NPL];
   float minA = 3.0e38f;  // smallest |A| of my real states
 #pragma unroll
   for (int j = 0; j < NPL; ++j) {
@@ -357,28 +357,54 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
     if (dvalid && real) A = -expf(a.A_log[(size_t)d * N + n]);
     A = fminf(A, -kMinAbsA);
     if (real) minA = fminf(minA, -A);
+    Av[j] = A;
     const float ak = real ? (PRECISE ? A : A * kLog2e) : 0.0f;
     const float ik = real ? 1.0f / A : 0.0f;
-    float hin = 0.0f;
-    if (!AGG && real && dvalid) {
-      if (a.h0) hin = a.h0[((size_t)b * Dm + d) * N + n];
-      for (int k = 0; k < seg; ++k) {
-        const size_t row = (size_t)b * (a.nseg - 1) + k;
-        const float ds = a.agg_dsum[row * Dm + d];
-        const float decay = PRECISE ? expf(A * ds) : hw_ex2(ak * ds);
-        hin = fmaf(decay, hin, a.agg_h[(row * Dm + d) * N + n]);
-      }
-    }
-    const float sv = SCALED ? hin * A : hin;
+    hin[j] = (!AGG && real && dvalid && a.h0) ? a.h0[((size_t)b * Dm + d) * N + n] : 0.0f;
     if (j % 2 == 0) {
       Ak[j / 2].x = ak;
       Ik[j / 2].x = ik;
-      st[j / 2].x = sv;
     } else {
       Ak[j / 2].y = ak;
       Ik[j / 2].y = ik;
-      st[j / 2].y = sv;
     }
+  }
+  // Initial state of my segment: h0 (or 0) composed with the aggregates of
+  // the earlier segments, oldest first. The segments are the outer loop and
+  // my NPL aggregate values are read as 16-byte vectors where N allows, so
+  // that the loads of several segments are in flight at once (they do not
+  // depend on the state being composed).
+  if (!AGG && dvalid && seg > 0) {
+    const bool vec = (N % 4) == 0 && (q + 1) * NPL <= N;  // all my states real: the vectors stay in the row
+#pragma unroll 4
+    for (int k = 0; k < seg; ++k) {
+      const size_t row = (size_t)b * (a.nseg - 1) + k;
+      const float ds = a.agg_dsum[row * Dm + d];
+      const float* ah = a.agg_h + (row * Dm + d) * N + q * NPL;
+      float e[NPL];
+#pragma unroll
+      for (int j = 0; j < NPL; j += 4) {
+        if (vec) {
+          const float4 v = *reinterpret_cast<const float4*>(ah + j);
+          e[j] = v.x; e[j + 1] = v.y; e[j + 2] = v.z; e[j + 3] = v.w;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) e[j + i] = (q * NPL + j + i < N) ? ah[j + i] : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < NPL; ++j) {
+        const float ak = (j % 2 == 0) ? Ak[j / 2].x : Ak[j / 2].y;
+        const float decay = PRECISE ? expf(Av[j] * ds) : hw_ex2(ak * ds);
+        hin[j] = fmaf(decay, hin[j], e[j]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const float sv = SCALED ? hin[j] * Av[j] : hin[j];
+    if (j % 2 == 0) st[j / 2].x = sv;
+    else st[j / 2].y = sv;
   }
   const float bias = chan_bias[c];
   const float Dd = chan_D[c];
