@@ -180,6 +180,21 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+def stored_traffic(workload, chosen):
+    """DRAM bytes per scan call from the committed ncu summary of this workload,
+    if it was taken on the same plan and the current kernel sources."""
+    if workload is None or not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu summary for this workload and plan"
+    with open(TRAFFIC_FILE) as f:
+        tr = json.load(f).get(workload)
+    if not tr or getattr(chosen, "time_lanes", 0) > 1:
+        return None, "no ncu summary for this workload and plan"
+    if tr.get("plan") == [chosen.lanes_per_channel, chosen.segments] and \
+            tr.get("kernel_source_sha") == kernel_source_sha():
+        return tr.get("dram_bytes_per_call"), tr.get("source")
+    return None, "ncu summary is for another plan or an older kernel"
+
+
 def measure_decode(device, stream, peaks, calls=200, which=("decode", "decode128")):
     """Decode step on the full decode workloads (B128 D5120, N = 16 and 128): us per call and GB/s.
 
@@ -302,10 +317,12 @@ def measure_layer(name, device, stream, peaks, sms, calls=50, seed=0, time_lanes
     assert binding.mamba_device_status() == 0, "a kernel reported a timeout"
     ms = e0.elapsed_time(e1) / calls
     f = scan_figures(cfg, ms, sms, peaks)
+    traffic, traffic_note = stored_traffic(name, chosen)
     del sets, graphs, base
     torch.cuda.empty_cache()
     return {"workload": cfg.description, "kernel_ms": ms, "channel_steps_per_s": B * Dm * L / (ms / 1e3),
-            "hbm": {"achieved": f["gbs"], "unit": "GB/s", "frac": f["hbm_frac"], "bytes_per_call": f["alg_bytes"]},
+            "hbm": {"achieved": f["gbs"], "unit": "GB/s", "frac": f["hbm_frac"], "bytes_per_call": f["alg_bytes"],
+                    "traffic": traffic, "traffic_source": traffic_note},
             "alu": {"achieved": f["tops"], "unit": "T FP32 lane-op/s", "frac": f["alu_frac"],
                     "ops_per_call": f["alg_ops"]},
             "plan": {"lanes_per_channel": chosen.lanes_per_channel, "segments": chosen.segments,
@@ -518,15 +535,7 @@ def run_ours(args, rank, world, device):
     alg_bytes, alg_ops, peak_tops = fig["alg_bytes"], fig["alg_ops"], fig["peak_tops"]
     achieved_tops, achieved_gbs = fig["tops"], fig["gbs"]
     clocks = sampler.summary(t_wall0, t_wall1)
-    traffic, traffic_note = None, "no ncu summary for this workload and plan"
-    if os.path.exists(TRAFFIC_FILE):
-        with open(TRAFFIC_FILE) as f:
-            tr = json.load(f).get(args.workload) if args.seqlen == 0 else None
-        if tr and tr.get("plan") == [chosen.lanes_per_channel, chosen.segments] and \
-                tr.get("kernel_source_sha") == kernel_source_sha():
-            traffic, traffic_note = tr.get("dram_bytes_per_call"), tr.get("source")
-        elif tr:
-            traffic_note = "ncu summary is for another plan or an older kernel"
+    traffic, traffic_note = stored_traffic(args.workload if args.seqlen == 0 else None, chosen)
     decode = None if args.no_decode else measure_decode(device, stream, peaks, args.decode_calls, decode_names(args))
     # The same scan with the simplified discretisation (Bbar = dt B): 4 FP32 lane-ops per state.
     simple = None
