@@ -33,16 +33,17 @@
 // the recomputation (s_t = s_{t-1} + (abar - 1)(s_{t-1} + B u), so A h_{t-1} is
 // read directly); fp32 inputs use expm1f and the unscaled h, as the forward
 // does. dA_log is accumulated as
-//   dA_log = A sum_t lambda_t dt_t (abar h_{t-1} + dt_t phi'(dt A) B u),
-// phi(x) = (e^x - 1) / x, phi'(x) = (x e^x - e^x + 1) / x^2 taken from its
-// series below |x| = 1/8 and its closed form above. (The equivalent difference
-// dt abar lambda v - q lambda B u cancels to first order in dt A: an error of
-// the hardware exp(dt A) of size e becomes a relative error near 2 e / (dt A)^2
-// of the difference.) The A factor is taken out so that |A| below the
-// kernels' 1e-20 floor still gives the exact dA_log. abar - 1 (for q and the
-// recomputation) is ex2 - 1 unless a state of the warp has dt |A| < 2^-14 at
-// that step, when the step takes expm1_acc (a warp-uniform branch; fp32
-// inputs use expm1f throughout).
+//   dA_log = A sum_t lambda_t (dt_t abar h_{t-1} + w_t B u),
+// w = dq/dA = dt^2 phi'(dt A) for q = dt phi(dt A), phi(x) = (e^x - 1) / x,
+// taken from the series of phi' below |dt A| = 1/8 and as (dt abar - q) / A
+// above it. (The equivalent per-step difference dt abar lambda v - q lambda B u
+// cancels to first order in dt A: an error e of the hardware exp(dt A) becomes
+// a relative error near 2 e / (dt A)^2 of the difference.) The A factor is
+// applied at the end to the unfloored A, so that |A| below the kernels' 1e-20
+// floor still gives the exact dA_log. abar - 1 (for q and the recomputation)
+// is ex2 - 1 unless a channel of the CTA has a step with dt |A| < 2^-14 in the
+// chunk, when the whole chunk takes expm1_acc (a CTA-uniform choice made where
+// the chunk's dt are computed; fp32 inputs use expm1f throughout).
 //
 // Time segments (for small batch x channels over long sequences): the
 // sequence is cut into S segments of whole chunks, one CTA per (channel
@@ -98,8 +99,8 @@ struct BwdGeom {
   static constexpr size_t oBf = oRed + 3 * szF;                        // B, C as float
   static constexpr int NW = kBwdThreads / 32;
   static constexpr size_t oAcc = oBf + 2 * size_t(K) * N * 4;          // [warps][K][2N] dB | dC of the chunk
-  static constexpr size_t oCh = oAcc + size_t(NW) * K * 2 * N * 4;     // per-channel bias, D
-  static constexpr size_t oHist = align16(oCh + 2 * size_t(CB) * 4);   // [K+1][threads] states
+  static constexpr size_t oCh = oAcc + size_t(NW) * K * 2 * N * 4;     // per-channel bias, D, accurate-path bound
+  static constexpr size_t oHist = align16(oCh + 3 * size_t(CB) * 4);   // [K+1][threads] states
   static constexpr size_t kSmem = oHist + size_t(K + 1) * kBwdThreads * 16;
   static_assert(N % 16 == 0 && LPC <= 32, "state size must be 16, 32, 64 or 128");
   static_assert((CB * ES) % SBX == 0 && (N * ES) % SBB == 0, "slot width must divide a tile row");
@@ -217,26 +218,14 @@ __device__ __forceinline__ void fwd_step_precise(float (&h)[4], float4 B4, float
   }
 }
 
-// phi'(x) for phi(x) = (e^x - 1) / x, x <= 0, given xl = x log2(e), e = e^x,
-// em1 = e^x - 1 (accurate) and ix = 1 / x: the series 1/2 + x/3 + x^2/8 + x^3/30
-// below |x| = 1/8 (truncation error below x^4 / 144 / (1/2) < 6e-7 relative),
-// (e - em1 ix) ix above it.
-__device__ __forceinline__ float dphi_acc(float xl, float e, float em1, float ix) {
-  const float x = xl * kLn2;
-  const float ser = fmaf(x, fmaf(x, fmaf(x, 1.0f / 30.0f, 1.0f / 8.0f), 1.0f / 3.0f), 0.5f);
-  return (fabsf(x) < 0.125f) ? ser : (e - em1 * ix) * ix;
-}
-
-// dphi_acc for a packed pair: both branches in f32x2 arithmetic, one select per element.
-__device__ __forceinline__ float2 dphi_acc2(float2 xl, float2 e, float2 em1, float2 ix) {
-  const float2 x = __fmul2_rn(xl, make_float2(kLn2, kLn2));
-  const float2 ser = __ffma2_rn(x, __ffma2_rn(x, __ffma2_rn(x, make_float2(1.0f / 30.0f, 1.0f / 30.0f),
-                                                          make_float2(1.0f / 8.0f, 1.0f / 8.0f)),
-                                            make_float2(1.0f / 3.0f, 1.0f / 3.0f)),
-                                make_float2(0.5f, 0.5f));
-  const float2 closed = __fmul2_rn(__ffma2_rn(make_float2(-em1.x, -em1.y), ix, e), ix);
-  return make_float2(fabsf(x.x) < 0.125f ? ser.x : closed.x, fabsf(x.y) < 0.125f ? ser.y : closed.y);
-}
+// Series of phi'(x) for phi(x) = (e^x - 1) / x in xl = x log2(e):
+// 1/2 + x/3 + x^2/8 + x^3/30 with the powers of ln 2 folded into the
+// coefficients (truncation error below x^4 / 144, relative to phi' >= 0.44,
+// under 4e-7 for |x| < 1/8).
+constexpr float kDphi1 = 0.23104906018664842f;   // ln2 / 3
+constexpr float kDphi2 = 0.060056142f;           // ln2^2 / 8
+constexpr float kDphi3 = 0.011100426f;           // ln2^3 / 30
+constexpr float kDphiSeriesMaxXl = 0.18033688f;  // |x| = 1/8 in units of x log2(e)
 
 // ---------------------------------------------------- adjoint step (4 states)
 // Given s_t (sn), s_{t-1} (sp) and lambda_{t+1} abar_{t+1} (carry): updates
@@ -244,15 +233,19 @@ __device__ __forceinline__ float2 dphi_acc2(float2 xl, float2 e, float2 em1, flo
 // v[0..3] and the dC partials to v[4..7], and returns the sums over the 4
 // states of the du, dt and y terms.
 // ACC selects abar - 1: ex2 - 1 (false) or expm1_acc (true). The dA_log terms
-// (without their A factor) go to G.
+// go to two sums without their A factor: Gs collects dt abar lambda s_{t-1}
+// (times 1 / A at the end, giving dt abar lambda h_{t-1}) and Gw collects
+// w lambda B u with w = dt^2 phi'(dt A), the derivative of q = dt phi(dt A)
+// with respect to A: dt^2 times the series below |dt A| = 1/8, and
+// (dt abar - q) / A (no cancellation there) above it.
 template <int DISC, bool ACC>
 __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, float4 C4, float dt, float uu, float dy,
-                                              float2 (&carry)[2], float2 (&G)[2], const float2 (&Al)[2],
-                                              const float2 (&Ik)[2], float (&v)[8], float& dus, float& ddt,
-                                              float& ys) {
+                                              float2 (&carry)[2], float2 (&Gs)[2], float2 (&Gw)[2],
+                                              const float2 (&Al)[2], const float2 (&Ik)[2], const float2 (&nIk)[2],
+                                              float (&v)[8], float& dus, float& ddt, float& ys) {
   const float2 dd = dup2(dt), u2 = dup2(uu), yy = dup2(dy);
+  [[maybe_unused]] const float2 dt2 = dup2(dt * dt), ndd = dup2(-dt);
   float2 sdus = make_float2(0.f, 0.f), sddt = sdus, sys = sdus;
-  [[maybe_unused]] const float rdt = DISC == 0 ? hw_rcp(dt) : 0.0f;  // 1 / dt (dt = 0 only where |x| < 1/8)
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float2 Bp = h == 0 ? lo2(B4) : hi2(B4);
@@ -267,26 +260,27 @@ __device__ __forceinline__ void adj_step_fast(float4 sn, float4 sp, float4 B4, f
     const float2 ab = ex2_2(x);
     const float2 Bu = __fmul2_rn(Bp, u2);
     const float2 al = __fmul2_rn(ab, lam);
-    float2 r, m;
+    float2 r;
     if (DISC == 0) {
       const float2 em1 = ACC ? make_float2(expm1_acc(x.x, ab.x), expm1_acc(x.y, ab.y))
                              : __fadd2_rn(ab, make_float2(-1.f, -1.f));
       const float2 q = __fmul2_rn(em1, Ik[h]);                 // (abar - 1) / A
       r = __fmul2_rn(lam, q);
-      m = __fmul2_rn(al, __fadd2_rn(spp, Bu));                  // abar lambda (A h_{t-1} + B u)
-      const float2 ix = __fmul2_rn(Ik[h], dup2(rdt));           // 1 / (dt A)
-      const float2 dp = dphi_acc2(x, ab, em1, ix);
-      const float2 hp = __fmul2_rn(spp, Ik[h]);                 // h_{t-1}
-      const float2 inner = __ffma2_rn(al, hp, __fmul2_rn(__fmul2_rn(dd, dp), __fmul2_rn(lam, Bu)));
-      G[h] = __ffma2_rn(dd, inner, G[h]);                       // dt (abar h + dt phi' B u) lambda
+      sddt = __ffma2_rn(al, __fadd2_rn(spp, Bu), sddt);       // abar lambda (A h_{t-1} + B u)
+      Gs[h] = __ffma2_rn(__fmul2_rn(dd, al), spp, Gs[h]);
+      const float2 ser = __fmul2_rn(
+          __ffma2_rn(x, __ffma2_rn(x, __ffma2_rn(x, dup2(kDphi3), dup2(kDphi2)), dup2(kDphi1)), dup2(0.5f)), dt2);
+      const float2 clo = __fmul2_rn(__ffma2_rn(ndd, ab, q), nIk[h]);  // (dt abar - q) / A
+      const float2 w = make_float2(fabsf(x.x) < kDphiSeriesMaxXl ? ser.x : clo.x,
+                                   fabsf(x.y) < kDphiSeriesMaxXl ? ser.y : clo.y);
+      Gw[h] = __ffma2_rn(w, __fmul2_rn(lam, Bu), Gw[h]);
     } else {
       r = __fmul2_rn(lam, dd);
-      m = __ffma2_rn(al, spp, __fmul2_rn(lam, Bu));             // lambda (abar A h_{t-1} + B u)
-      G[h] = __ffma2_rn(__fmul2_rn(dd, al), __fmul2_rn(spp, Ik[h]), G[h]);  // dt abar lambda h_{t-1}
+      sddt = __ffma2_rn(al, spp, __ffma2_rn(lam, Bu, sddt));  // lambda (abar A h_{t-1} + B u)
+      Gs[h] = __ffma2_rn(__fmul2_rn(dd, al), spp, Gs[h]);     // dt abar lambda A h_{t-1}
     }
     const float2 db = __fmul2_rn(r, u2);
     sdus = __ffma2_rn(r, Bp, sdus);
-    sddt = __fadd2_rn(sddt, m);
     carry[h] = al;
     v[2 * h] = db.x;
     v[2 * h + 1] = db.y;
@@ -366,6 +360,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   float* acc = reinterpret_cast<float*>(sm + G::oAcc);
   float* ch_bias = reinterpret_cast<float*>(sm + G::oCh);
   float* ch_D = ch_bias + CB;
+  float* ch_thr = ch_D + CB;
   float4* hist = reinterpret_cast<float4*>(sm + G::oHist);
 
   const int tid = threadIdx.x, lane = tid & 31;
@@ -395,7 +390,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   // A = -exp(A_log) with |A| >= kMinAbsA, 1/A and (fast path) A log2(e) for my
   // states; Atrue keeps A unfloored for the final dA_log = A dloss/dA.
   float A[NPL], Ik[NPL], Atrue[NPL];
-  float2 A2[2], Al2[2], Ik2[2];
+  float2 A2[2], Al2[2], Ik2[2], nIk2[2];
   float minA = 3.0e38f;  // smallest |A| of my channel's states
 #pragma unroll
   for (int k = 0; k < NPL; ++k) {
@@ -407,13 +402,17 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
   }
 #pragma unroll
   for (int o = 1; o < LPC; o <<= 1) minA = fminf(minA, __shfl_xor_sync(0xffffffffu, minA, o));
-  // dt below which a step of my channel needs the accurate form (bf16 inputs)
-  const float thr = kBwdFastMinDtA / minA;
+  // dt below which a step of my channel needs the accurate form (bf16
+  // inputs). A chunk in which any channel of the CTA meets such a step runs
+  // all of its steps with the accurate abar - 1 (a CTA-uniform choice made
+  // where the chunk's dt are computed).
+  if (part == 0) ch_thr[c] = cv ? kBwdFastMinDtA / minA : 0.0f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     A2[h] = make_float2(A[2 * h], A[2 * h + 1]);
     Al2[h] = make_float2(A[2 * h] * kLog2e, A[2 * h + 1] * kLog2e);
     Ik2[h] = make_float2(Ik[2 * h], Ik[2 * h + 1]);
+    nIk2[h] = make_float2(-Ik[2 * h], -Ik[2 * h + 1]);
   }
 
   // state: h (fp32 inputs) or s = A h as two pairs (bf16 inputs)
@@ -435,17 +434,17 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     if constexpr (PRECISE) return make_float4(hs[0], hs[1], hs[2], hs[3]);
     else return make_float4(s2[0].x * Ik[0], s2[0].y * Ik[1], s2[1].x * Ik[2], s2[1].y * Ik[3]);
   };
-  // One forward step; the fast bf16 form unless a lane of the warp has
-  // dt |A| < 2^-12 (a warp-uniform choice; dt = 0 marks steps past the end).
-  auto fwd_step = [&](float4 B4, float dt, float uu) {
-    if constexpr (PRECISE) {
+  // One forward step; ACC takes the accurate abar - 1 (bf16 inputs).
+  auto fwd_step = [&](auto accv, float4 B4, float dt, float uu) {
+    if constexpr (PRECISE)
       fwd_step_precise<DISC>(hs, B4, dt, uu, A, Ik);
-    } else {
-      if (__all_sync(0xffffffffu, dt >= thr || dt == 0.0f))
-        fwd_step_fast<DISC, false>(s2, B4, dt, uu, Al2, A2);
-      else
-        fwd_step_fast<DISC, true>(s2, B4, dt, uu, Al2, A2);
-    }
+    else
+      fwd_step_fast<DISC, decltype(accv)::value>(s2, B4, dt, uu, Al2, A2);
+  };
+  // Runs f(std::true_type) if on, else f(std::false_type).
+  auto with_acc = [](bool on, auto&& f) {
+    if (on) f(std::true_type{});
+    else f(std::false_type{});
   };
 
   // Exponential decay of my states over a segment with the given sum of dt.
@@ -490,22 +489,26 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
         xp.load(src_x, rowb + (ci + 1) * K, Dm, d0, nch, rows_of(ci + 1), tid);
         bp.load(src_b, rowb + (ci + 1) * K, N, 0, N, rows_of(ci + 1), tid);
       }
+      bool need = false;  // a step of the chunk needs the accurate form
       for (int p = tid; p < K * CB; p += kBwdThreads) {
         const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
         const bool live = p / CB < tv;  // rows past the segment are exact no-ops
-        f_tc[p] = make_float4(live ? (PRECISE ? softplus_precise(x) : softplus_fast(x)) : 0.0f,
-                              live ? E::load(xs + p) : 0.0f, 0.f, 0.f);
+        const float dt = live ? (PRECISE ? softplus_precise(x) : softplus_fast(x)) : 0.0f;
+        need |= live && dt < ch_thr[p % CB];
+        f_tc[p] = make_float4(dt, live ? E::load(xs + p) : 0.0f, 0.f, 0.f);
       }
       for (int p = tid; p < K * N; p += kBwdThreads) f_B[p] = E::load(bs + p);
-      __syncthreads();
+      const bool exact = __syncthreads_or(need) != 0;
+      with_acc(exact, [&](auto accv) {
 #pragma unroll 4
-      for (int t = 0; t < K; ++t) {
-        const float4 tc = f_tc[t * CB + c];
-        fwd_step(ld4(f_B + t * N + n0), tc.x, tc.y);
-        if constexpr (MODE == kBwdFwdAgg) {
-          if (PRECISE) dsum_d += tc.x; else dsum += tc.x;
+        for (int t = 0; t < K; ++t) {
+          const float4 tc = f_tc[t * CB + c];
+          fwd_step(accv, ld4(f_B + t * N + n0), tc.x, tc.y);
+          if constexpr (MODE == kBwdFwdAgg) {
+            if (PRECISE) dsum_d += tc.x; else dsum += tc.x;
+          }
         }
-      }
+      });
     }
     if constexpr (MODE == kBwdFwdAgg) {
       if (cv) {
@@ -518,7 +521,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
 
   // --------------------------------------------------- phase 2: adjoint
   float carry[NPL], dAl[NPL] = {0.f, 0.f, 0.f, 0.f};  // fp32 inputs (dAl: without the A factor)
-  float2 carry2[2], G2[2];                            // bf16 inputs (G2: dA_log terms without the A factor)
+  float2 carry2[2], Gs2[2], Gw2[2];                   // bf16 inputs (dA_log sums, see adj_step_fast)
   {
     float4 g = (MODE == kBwdFull && cv && a.dlast) ? ld4(a.dlast + ((size_t)b * Dm + d) * N + n0) : zero4;
     if constexpr (MODE == kBwdFull) {
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     carry[0] = g.x; carry[1] = g.y; carry[2] = g.z; carry[3] = g.w;
     carry2[0] = lo2(g);
     carry2[1] = hi2(g);  // (kBwdAdjAgg runs on the scalar carry for either input type)
-    G2[0] = G2[1] = make_float2(0.f, 0.f);
+    Gs2[0] = Gs2[1] = Gw2[0] = Gw2[1] = make_float2(0.f, 0.f);
   }
   float dD_acc = 0.0f, dbias_acc = 0.0f;  // channel d0 + tid % CB
   XCopy4 xq;
@@ -563,10 +566,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       bq.load(src_bc, rowb + t0 - K, N, 0, N, K, tid);
       if (MODE == kBwdFull && cv) ckn = ld4(ckp + (ci - 1) * ck_stride);
     }
+    bool need = false;  // a step of the chunk needs the accurate form
     for (int p = tid; p < K * CB; p += kBwdThreads) {
       const float x = E::load(xs + K * CB + p) + ch_bias[p % CB];
       const float g = E::load(xs + 3 * K * CB + p);
       const float dt = PRECISE ? softplus_precise(x) : softplus_fast(x);
+      need |= p / CB < tv && dt < ch_thr[p % CB];
       const float sg = PRECISE ? sigmoid_precise(x) : sigmoid_fast(x);
       float dy = g;
       if (has_z) {
@@ -581,7 +586,7 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       f_B[p] = E::load(bs + p);
       f_C[p] = E::load(bs + K * N + p);
     }
-    __syncthreads();
+    const bool exact = __syncthreads_or(need) != 0;
 
     if constexpr (MODE == kBwdAdjAgg) {
       // only the adjoint: lambda_t = dy_t C_t + carry, carry <- abar_t lambda_t
@@ -604,18 +609,18 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
     // loads, which the compiler cannot prove independent.)
     load_state(cks);
     hist[tid] = state4();
-    {
+    with_acc(exact, [&](auto accv) {
       float4 tc = f_tc[c], B4 = ld4(f_B + n0);
 #pragma unroll 2
       for (int t = 0; t < tv; ++t) {
         const int tn = t + 1 < tv ? t + 1 : t;
         const float4 tc_n = f_tc[tn * CB + c], B4_n = ld4(f_B + tn * N + n0);
-        fwd_step(B4, tc.x, tc.y);
+        fwd_step(accv, B4, tc.x, tc.y);
         hist[(t + 1) * kBwdThreads + tid] = state4();
         tc = tc_n;
         B4 = B4_n;
       }
-    }
+    });
 
     // adjoint, backwards through the chunk, G::SBT steps per round of reductions
     constexpr int SBT = G::SBT, VPL = G::VPL;
@@ -635,10 +640,12 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
           const float4 B4 = ld4(f_B + t * N + n0), C4 = ld4(f_C + t * N + n0);
           if constexpr (PRECISE)
             adj_step_precise<DISC>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry, dAl, A, Ik, v, dus, ddt, ys);
-          else if (__all_sync(0xffffffffu, tc.x >= thr))
-            adj_step_fast<DISC, false>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, G2, Al2, Ik2, v, dus, ddt, ys);
+          else if (exact)
+            adj_step_fast<DISC, true>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, Gs2, Gw2, Al2, Ik2, nIk2, v, dus,
+                                      ddt, ys);
           else
-            adj_step_fast<DISC, true>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, G2, Al2, Ik2, v, dus, ddt, ys);
+            adj_step_fast<DISC, false>(sn, sp, B4, C4, tc.x, tc.y, tc.z, carry2, Gs2, Gw2, Al2, Ik2, nIk2, v, dus,
+                                       ddt, ys);
           sn = sp;
         }
 #pragma unroll
@@ -715,7 +722,15 @@ __global__ void __launch_bounds__(kBwdThreads, 3) scan_bwd_kernel(const BwdArgs 
       dA4 = make_float4(Atrue[0] * dAl[0], Atrue[1] * dAl[1], Atrue[2] * dAl[2], Atrue[3] * dAl[3]);
       g4 = make_float4(carry[0], carry[1], carry[2], carry[3]);
     } else {
-      dA4 = make_float4(Atrue[0] * G2[0].x, Atrue[1] * G2[0].y, Atrue[2] * G2[1].x, Atrue[3] * G2[1].y);
+      // dA_log = A sum dt lambda (abar h_{t-1} + dt phi' B u), the first term from A h_{t-1} times 1 / A
+      float G[NPL];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 g = __ffma2_rn(Gs2[h], Ik2[h], Gw2[h]);
+        G[2 * h] = g.x;
+        G[2 * h + 1] = g.y;
+      }
+      dA4 = make_float4(Atrue[0] * G[0], Atrue[1] * G[1], Atrue[2] * G[2], Atrue[3] * G[3]);
       g4 = make_float4(carry2[0].x, carry2[0].y, carry2[1].x, carry2[1].y);
     }
     atomicAdd(reinterpret_cast<float4*>(a.dA_log + (size_t)d * N + n0), dA4);
