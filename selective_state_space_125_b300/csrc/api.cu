@@ -427,6 +427,7 @@ mamba_status_t scan_fwd_impl(int batch, int dim, int dstate, int seqlen, mamba_d
       return cuda_fail(e, "scan aggregate pass launch");
     }
   }
+  a.after_agg = plan.nseg > 1 ? 1 : 0;
   cudaError_t e = launch(ScanMode::kFull, plan.nseg);
   if (work) {
     cudaError_t e2 = cudaFreeAsync(work, stream);

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace mamba {
 
 // Kernels never trap: a bounded wait that runs out records kStatusTimeout in
@@ -38,6 +40,34 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void record_status(int* word, int code) {
   if (word) atomicCAS(word, 0, code);
+}
+
+// Programmatic dependent launch (sm_90 and later). A kernel launched with the
+// programmatic-stream-serialization attribute may start while the kernel
+// before it in the stream is still running; griddep_wait() blocks the calling
+// thread until that kernel has completed and its memory is visible, so every
+// thread calls it before its first global-memory access. griddep_launch()
+// lets the next such kernel in the stream start early (it still waits).
+// Both are no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launches kernel<<<grid, block, smem, stream>>>(args...) with programmatic
+// stream serialization allowed.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ unsigned long long global_timer_ns() {

@@ -33,6 +33,8 @@ struct ScanArgs {
   const float* conv_b;      // (D) or null
   int conv_width;           // 1..4
   unsigned long long wait_ns;  // limit of the pipeline's mbarrier waits (ns); 0 gives up at once
+  int after_agg;            // full pass launched right after the aggregate pass, with programmatic
+                            // stream serialization: it may start early and waits before reading agg_*
 };
 
 struct ScanMaps {

@@ -297,6 +297,9 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   const Tin* gz = static_cast<const Tin*>(a.z);
   const Tin* gB = static_cast<const Tin*>(a.B);
   const Tin* gC = static_cast<const Tin*>(a.C);
+  // The next kernel in the stream may start its prologue while this grid runs
+  // (it waits before it reads what this grid writes).
+  griddep_launch();
 
   // Per-channel constants of this CTA.
   for (int i = tid; i < CB; i += kScanThreads) {
@@ -374,6 +377,10 @@ __global__ void __launch_bounds__(kScanThreads, ScanMinBlocks<NPL>::value)
   // my NPL aggregate values are read as 16-byte vectors where N allows, so
   // that the loads of several segments are in flight at once (they do not
   // depend on the state being composed).
+  // A full pass that follows the aggregate pass may have started before that
+  // pass ended: it has staged its first chunks of inputs (which the aggregate
+  // pass does not write) and now waits for the aggregates.
+  if (!AGG && a.after_agg && seg > 0) griddep_wait();
   if (!AGG && dvalid && seg > 0) {
     const bool vec = (N % 4) == 0 && (q + 1) * NPL <= N;  // all my states real: the vectors stay in the row
 #pragma unroll 4
@@ -642,6 +649,7 @@ cudaError_t launch_scan_variant(ScanMode mode, const ScanArgs& a, const ScanMaps
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  if (mode == ScanMode::kFull && a.after_agg) return launch_pdl(kfull, grid, dim3(kScanThreads), G::kSmem, stream, a, maps);
   if (mode == ScanMode::kFull)
     kfull<<<grid, kScanThreads, G::kSmem, stream>>>(a, maps);
   else

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
   const int N = a.dstate;
   const int b0 = blockIdx.y * kDecodeRows;
   const int dd = dvalid ? d : 0;
+  griddep_launch();
+  griddep_wait();
 
   // Per-channel constants for my states: Al = A (precise) or A log2(e) (fast), Ik = 1 / A.
   float Al[MAXG][4], Ik[MAXG][4];
@@ -317,6 +319,8 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
+  griddep_launch();
+  griddep_wait();
   __syncthreads();
   int issued = 0;  // thread 0
   if (tid == 0)
@@ -456,8 +460,8 @@ static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, bool one_wave, in
   const int blocks_x = (a.dim + G::kCBD - 1) / G::kCBD;
   const int groups = one_wave ? occupancy * sms / blocks_x : (ctas_per_sm * sms + blocks_x - 1) / blocks_x;
   const int rb = std::max(1, std::min(a.batch, groups));
-  state_update_bulk_kernel<Tin, TPC, DISC, S><<<dim3(blocks_x, rb), kBulkThreads, G::kSmem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(state_update_bulk_kernel<Tin, TPC, DISC, S>, dim3(blocks_x, rb), dim3(kBulkThreads), G::kSmem,
+                    stream, a);
 }
 
 // Ring depth and grid, from sweeps on B300 (batch 128, dim 5120, 3-12 stages,
@@ -497,11 +501,8 @@ template <typename Tin, int LPD, int MAXG>
 static cudaError_t launch_decode_lpd(const DecodeArgs& a, bool vec, cudaStream_t stream) {
   const int per_block = kDecodeThreads / LPD;
   const dim3 grid(unsigned((a.dim + per_block - 1) / per_block), unsigned((a.batch + kDecodeRows - 1) / kDecodeRows));
-  if (vec)
-    state_update_kernel<Tin, LPD, MAXG, true><<<grid, kDecodeThreads, 0, stream>>>(a);
-  else
-    state_update_kernel<Tin, LPD, MAXG, false><<<grid, kDecodeThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  if (vec) return launch_pdl(state_update_kernel<Tin, LPD, MAXG, true>, grid, dim3(kDecodeThreads), 0, stream, a);
+  return launch_pdl(state_update_kernel<Tin, LPD, MAXG, false>, grid, dim3(kDecodeThreads), 0, stream, a);
 }
 
 template <typename Tin>

@@ -124,11 +124,12 @@ def test_small_dt_leaves_state(dev, dtype):
     assert parity_err(outs, routs) <= TOL[dtype]
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("name", ["decode", "decode128"])
-def test_full_size_decode_sampled(dev, name):
+def test_full_size_decode_sampled(dev, name, seed):
     """All 1024 calls on the full (128, 5120, N) state; the oracle follows sampled channels."""
     cfg = DECODE_CONFIGS[name]
-    inp = make_decode_config_inputs(cfg, seed=0)
+    inp = make_decode_config_inputs(cfg, seed=seed)
     bsel = np.array([0, 63, 127])
     dsel = np.unique(np.concatenate([[0, cfg.dim - 1], np.random.default_rng(7).integers(0, cfg.dim, 62)]))
     st, outs = run_decode(inp, dev, cfg.steps, bsel=bsel, dsel=dsel)

@@ -175,10 +175,11 @@ def sampled_oracle(inp, bs, ds):
                                  sub["z"], sub["delta_bias"])
 
 
+@pytest.mark.parametrize("seed", [0, 1, 2])
 @pytest.mark.parametrize("name", ["m130", "m1p4b", "long"])
-def test_full_size_configs_sampled(dev, name):
+def test_full_size_configs_sampled(dev, name, seed):
     cfg = SCAN_CONFIGS[name]
-    inp = make_config_inputs(cfg, seed=0)
+    inp = make_config_inputs(cfg, seed=seed)
     out, last = run_gpu(inp, dev)
     rng = np.random.default_rng(123)
     bs = np.unique(np.concatenate([[0, cfg.batch - 1], rng.integers(0, cfg.batch, 2)]))
