@@ -36,6 +36,14 @@
  *     arguments were valid and the kernels were launched. A fault inside a
  *     kernel shows at the caller's next synchronisation, or through
  *     mamba_device_status().
+ *   - Stream order holds for every byte read or written. The decode kernels,
+ *     and the scan's second kernel when a call launches two, use programmatic
+ *     dependent launch: such a kernel may become resident while the kernel
+ *     before it in the stream is still running, but each of its threads waits
+ *     for that kernel to complete and flush (griddepcontrol.wait) before it
+ *     touches memory that kernel may write. The scan and decode kernels also
+ *     let the next kernel in the stream launch early; a kernel launched
+ *     without the programmatic attribute is not affected by that.
  *   - Validation happens before any launch. Every failure returns a status
  *     and sets a thread-local detail string (mamba_last_error_detail()).
  *     No C++ exception crosses the ABI.
@@ -48,10 +56,11 @@
  *     fp32 with fp32 state. With MAMBA_F32 inputs the kernels use accurate
  *     expm1/exp/log1p; with MAMBA_BF16 inputs they use the hardware ex2/lg2
  *     approximations, and take exp(dt A) - 1 from a short series wherever
- *     dt |A| is small enough that ex2 - 1 would cancel (the scan and the
- *     backward switch per chunk or step when some state of the block falls
- *     below dt |A| = 2^-14 or 2^-12; the decode step always does), so that
- *     Bbar keeps a relative error near 1e-6 at any dt A.
+ *     dt |A| is small enough that ex2 - 1 would cancel (the scan reruns a
+ *     16-step chunk of a warp with the series when some step of it falls
+ *     below dt |A| = 2^-14; the backward takes the series for a whole chunk
+ *     of the CTA in that case; the decode step always does), so that Bbar
+ *     keeps a relative error near 1e-6 at any dt A.
  *   - |A| = exp(A_log) is floored at 1e-20 inside the kernels. At and below
  *     that floor exp(dt A) and (exp(dt A) - 1) / A equal their A -> 0 limits
  *     (1 and dt) in fp32 for any dt below 1e12, so results are those of the
