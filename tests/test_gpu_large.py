@@ -3,10 +3,10 @@
 Every global offset in the kernels is formed in 64-bit arithmetic and the
 TMA tensor maps take 64-bit extents and strides. These tests run a scan
 whose (B, L, D) activations hold about 2.18e9 elements each (4.4 GB in bf16,
-in the time-segmented plan the automatic planner picks there) and decode
-steps on a (B, D, N) state of about 2.15e9 fp32 values (8.6 GB), and check
-sampled channels against the oracle, including the last batch rows and
-channels whose offsets lie past 2^31.
+in the time-segmented plan the automatic planner picks there), the backward
+on the same shape, and decode steps on a (B, D, N) state of about 2.15e9 fp32
+values (8.6 GB), and check sampled channels against the oracle, including
+the last batch rows and channels whose offsets lie past 2^31.
 """
 import numpy as np
 import pytest
@@ -81,3 +81,36 @@ def test_decode_state_past_2_31_values(dev):
         routs.append(o)
     assert parity_err(got_state, rstate) <= TOL["bf16"]
     assert parity_err(np.stack(outs), np.stack(routs)) <= TOL["bf16"]
+
+
+def test_bwd_past_2_31_elements(dev):
+    """The backward on B8 L65536 D4160 bf16 (2.18e9 elements per activation and gradient tensor, an 8.7 GB
+    checkpoint workspace): every per-channel gradient of sampled channels against the oracle."""
+    import torch
+    from selective_state_space_125_b300 import binding
+    from selective_state_space_125_b300.workloads import make_bwd_inputs
+    batch, dim, n, L = 8, 4160, 16, 65536
+    inp = make_bwd_inputs(batch, dim, n, L, "bf16", seed=93)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
+    t = {k: to_torch(inp[k], "bf16", dev) for k in ("u", "delta", "z", "B", "C", "dout")}
+    g = binding.mamba_selective_scan_bwd(t["u"], t["delta"], f32(inp["A_log"]), t["B"], t["C"], t["dout"],
+                                         D=f32(inp["D"]), z=t["z"], delta_bias=f32(inp["delta_bias"]),
+                                         initial_state=f32(inp["h0"]), dlast_state=f32(inp["dlast"]))
+    torch.cuda.synchronize()
+    assert binding.mamba_device_status() == 0
+    chans = [0, 31, 32, 2047, 3000, dim - 2, dim - 1]
+    ci = torch.as_tensor(chans, device=dev)
+    got = {k: to_numpy(g[k][:, :, ci]) for k in ("du", "ddelta", "dz")}
+    got["dA_log"] = to_numpy(g["dA_log"])[chans]
+    got["dD"] = to_numpy(g["dD"])[chans]
+    got["ddelta_bias"] = to_numpy(g["ddelta_bias"])[chans]
+    got["dh0"] = to_numpy(g["dinitial_state"])[:, chans]
+    del t, g
+    sl = lambda a: np.ascontiguousarray(a[:, :, chans])
+    ref = oracle.selective_scan_bwd(sl(inp["u"]), sl(inp["delta"]), inp["A_log"][chans], inp["B"], inp["C"],
+                                    sl(inp["dout"]), D=inp["D"][chans], z=sl(inp["z"]),
+                                    delta_bias=inp["delta_bias"][chans], h0=inp["h0"][:, chans],
+                                    dlast=inp["dlast"][:, chans])
+    errs = {k: parity_err(got[k], ref[k]) for k in got}
+    bad = {k: e for k, e in errs.items() if not e <= TOL["bf16"]}
+    assert not bad, ", ".join(f"{k} {e:.2e}" for k, e in sorted(errs.items()))
