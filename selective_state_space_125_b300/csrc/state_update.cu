@@ -211,8 +211,13 @@ __global__ void __launch_bounds__(kDecodeThreads, DecodeMinBlocks<Tin, MAXG, VEC
 
 // ---------------------------------------------------------------------------
 // Bulk-staged decode step for the common layouts (N % 8 == 0, N <= 256,
-// dim % 8 == 0, 16-byte aligned pointers). A CTA owns a block of channels
-// and walks batch rows. For every row a 4- or 8-stage ring in shared memory receives,
+// dim % 8 == 0, 16-byte aligned pointers). The work is cut into units of one
+// batch row of one block of channels. On a 1-D grid (one wave) the units are
+// ordered block by block and each CTA walks a contiguous range of them, as
+// even as the grid allows, reloading its channels' constants where its range
+// enters the next block; on a 2-D grid CTA (x, y) walks rows y, y + gridDim.y,
+// ... of block x, so that the CTAs in flight touch neighbouring slabs of the
+// same rows. For every unit a 4- or 8-stage ring in shared memory receives,
 // by bulk copies that complete on an mbarrier, the row's state slab (8 KB)
 // and its u, delta, z, B, C. The threads update the slab in place (8 states
 // each), and one thread writes it back with a bulk store. Each thread
@@ -270,7 +275,9 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-template <typename Tin, int TPC, int DISC, int S>
+// BAL: the 1-D balanced layout (a contiguous range of units per CTA);
+// otherwise the 2-D one (rows blockIdx.y, + gridDim.y, ... of block blockIdx.x).
+template <typename Tin, int TPC, int DISC, int S, bool BAL>
 __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const DecodeArgs a) {
   using G = BulkGeom<Tin, TPC, S>;
   using E = Elem<Tin>;
@@ -292,19 +299,49 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
   const int tid = threadIdx.x;
   const int c = tid / TPC, part = tid % TPC;
   const int Dm = a.dim;
-  const int d0 = blockIdx.x * CBD;
-  const int nch = min(CBD, Dm - d0);
-  const int d = d0 + c;
-  const bool cvalid = c < nch;
-  const int rb = gridDim.y;
-  const int nrows = (a.batch - int(blockIdx.y) + rb - 1) / rb;  // rows blockIdx.y, + rb, ...
   const bool has_z = a.z != nullptr;
-  const uint32_t vec_bytes = uint32_t(nch * sizeof(Tin));
-  const uint32_t row_bytes = uint32_t(nch) * N * 4 + (has_z ? 3u : 2u) * vec_bytes + 2u * uint32_t(N * sizeof(Tin));
+  // This CTA's units, walked as (block, row) pairs from (blk0, row0): the
+  // next row of the same block, wrapping into the next block (BAL), or rows
+  // `step` apart within one block.
+  int blk0, row0, nrows, step;
+  if constexpr (BAL) {
+    const long long units = (long long)((Dm + CBD - 1) / CBD) * a.batch;  // u = block * batch + row
+    const long long u0 = units * blockIdx.x / gridDim.x;
+    nrows = int(units * (blockIdx.x + 1) / gridDim.x - u0);
+    blk0 = int(u0 / a.batch);
+    row0 = int(u0 - (long long)blk0 * a.batch);
+    step = 1;
+  } else {
+    blk0 = blockIdx.x;
+    row0 = blockIdx.y;
+    step = gridDim.y;
+    nrows = (a.batch - row0 + step - 1) / step;
+  }
+  int iss_blk = blk0, iss_row = row0;  // thread 0: the next unit to stage
+  // the 2-D layout's one block
+  const int nch_fixed = min(CBD, Dm - blk0 * CBD);
+  const uint32_t vec_fixed = uint32_t(nch_fixed * sizeof(Tin));
+  const uint32_t row_fixed =
+      uint32_t(nch_fixed) * N * 4 + (has_z ? 3u : 2u) * vec_fixed + 2u * uint32_t(N * sizeof(Tin));
 
-  auto issue = [&](int i) {  // thread 0: stage the row i of this CTA
+  auto issue = [&](int i) {  // thread 0: stage unit i of this CTA
     const int s = i % S;
-    const int b = int(blockIdx.y) + i * rb;
+    int b, d0;
+    if constexpr (BAL) {  // the unit (iss_blk, iss_row)
+      b = iss_row;
+      d0 = iss_blk * CBD;
+      if (++iss_row == a.batch) {
+        iss_row = 0;
+        ++iss_blk;
+      }
+    } else {
+      b = row0 + i * step;
+      d0 = blk0 * CBD;
+    }
+    const int nch = BAL ? min(CBD, Dm - d0) : nch_fixed;
+    const uint32_t vec_bytes = BAL ? uint32_t(nch * sizeof(Tin)) : vec_fixed;
+    const uint32_t row_bytes =
+        BAL ? uint32_t(nch) * N * 4 + (has_z ? 3u : 2u) * vec_bytes + 2u * uint32_t(N * sizeof(Tin)) : row_fixed;
     const size_t ch0 = (size_t)b * Dm + d0;
     mbar_arrive_expect_tx(&full[s], row_bytes);
     bulk_load(st_state(s), a.state + ch0 * N, uint32_t(nch) * N * 4, &full[s]);
@@ -326,29 +363,51 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(const D
   if (tid == 0)
     for (; issued < min(S - 1, nrows); ++issued) issue(issued);
 
-  // Constants of my channel's 8 states: A, 1 / A and A log2(e), the last two
-  // also as packed pairs for the bf16 path.
+  // Constants of my channel's 8 states in the current block: A, 1 / A and
+  // A log2(e), the last two also as packed pairs for the bf16 path.
   float Av[kBulkFloats], Ik[kBulkFloats];
   float2 A2[kBulkFloats / 2], Al2[kBulkFloats / 2], Ik2[kBulkFloats / 2];
   const int n0 = part * kBulkFloats;
+  int blk = -1, d0 = 0, d = 0;
+  bool cvalid = false;
+  float bias = 0.0f, Dd = 0.0f;
+  auto enter_block = [&](int nb) {
+    blk = nb;
+    d0 = nb * CBD;
+    d = d0 + c;
+    cvalid = c < min(CBD, Dm - d0);
 #pragma unroll
-  for (int i = 0; i < kBulkFloats; ++i) {
-    const float al = cvalid ? a.A_log[(size_t)d * N + n0 + i] : 0.0f;
-    Av[i] = fminf(PRECISE ? -expf(al) : -hw_ex2(al * kLog2e), -kMinAbsA);
-    Ik[i] = PRECISE ? 1.0f / Av[i] : hw_rcp(Av[i]);
-  }
+    for (int i = 0; i < kBulkFloats; ++i) {
+      const float al = cvalid ? a.A_log[(size_t)d * N + n0 + i] : 0.0f;
+      Av[i] = fminf(PRECISE ? -expf(al) : -hw_ex2(al * kLog2e), -kMinAbsA);
+      Ik[i] = PRECISE ? 1.0f / Av[i] : hw_rcp(Av[i]);
+    }
 #pragma unroll
-  for (int p = 0; p < kBulkFloats / 2; ++p) {
-    A2[p] = make_float2(Av[2 * p], Av[2 * p + 1]);
-    Al2[p] = make_float2(Av[2 * p] * kLog2e, Av[2 * p + 1] * kLog2e);
-    Ik2[p] = make_float2(Ik[2 * p], Ik[2 * p + 1]);
-  }
-  const float bias = (a.delta_bias && cvalid) ? a.delta_bias[d] : 0.0f;
-  const float Dd = (a.D && cvalid) ? a.D[d] : 0.0f;
+    for (int p = 0; p < kBulkFloats / 2; ++p) {
+      A2[p] = make_float2(Av[2 * p], Av[2 * p + 1]);
+      Al2[p] = make_float2(Av[2 * p] * kLog2e, Av[2 * p + 1] * kLog2e);
+      Ik2[p] = make_float2(Ik[2 * p], Ik[2 * p + 1]);
+    }
+    bias = (a.delta_bias && cvalid) ? a.delta_bias[d] : 0.0f;
+    Dd = (a.D && cvalid) ? a.D[d] : 0.0f;
+  };
 
+  if constexpr (!BAL) enter_block(blk0);
+  int cur_blk = blk0, b_bal = row0 - 1;  // (BAL) the unit of the iteration below
   for (int i = 0; i < nrows; ++i) {
     const int s = i % S;
-    const int b = int(blockIdx.y) + i * rb;
+    int b;
+    if constexpr (BAL) {
+      if (++b_bal == a.batch) {
+        b_bal = 0;
+        ++cur_blk;
+      }
+      if (cur_blk != blk) enter_block(cur_blk);  // uniform across the CTA
+      b = b_bal;
+    } else {
+      b = row0 + i * step;
+    }
+    const int nch = BAL ? min(CBD, Dm - d0) : nch_fixed;
     const bool ok = mbar_wait_bounded(&full[s], (i / S) & 1, a.wait_ns);
     if (__syncthreads_or(!ok)) {
       if (tid == 0) {
@@ -440,28 +499,35 @@ static bool decode_bulk_ok(const DecodeArgs& a) {
          al16(a.delta) && (!a.z || al16(a.z)) && al16(a.B) && al16(a.C);
 }
 
-// one_wave: as many row groups as fill every SM once at the kernel's
-// occupancy; otherwise enough row groups for about ctas_per_sm CTAs per SM.
-template <typename Tin, int TPC, int DISC, int S>
-static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, bool one_wave, int ctas_per_sm, cudaStream_t stream) {
+// BAL: a 1-D grid of one CTA per slot of every SM at the kernel's occupancy,
+// the units dealt out evenly (a CTA walks at most one unit more than
+// another); otherwise a 2-D grid of blocks x row groups, about ctas_per_sm
+// CTAs per SM.
+template <typename Tin, int TPC, int DISC, int S, bool BAL>
+static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, cudaStream_t stream) {
   using G = BulkGeom<Tin, TPC, S>;
   static int occupancy = 0;  // per instantiation; benign race (idempotent)
   if (occupancy == 0) {
-    cudaError_t e = cudaFuncSetAttribute(state_update_bulk_kernel<Tin, TPC, DISC, S>,
+    cudaError_t e = cudaFuncSetAttribute(state_update_bulk_kernel<Tin, TPC, DISC, S, BAL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, int(G::kSmem));
     int occ = 0;
     if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, state_update_bulk_kernel<Tin, TPC, DISC, S>,
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, state_update_bulk_kernel<Tin, TPC, DISC, S, BAL>,
                                                         kBulkThreads, G::kSmem);
     if (e != cudaSuccess) return e;
     occupancy = std::max(1, occ);
   }
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + G::kCBD - 1) / G::kCBD;
-  const int groups = one_wave ? occupancy * sms / blocks_x : (ctas_per_sm * sms + blocks_x - 1) / blocks_x;
-  const int rb = std::max(1, std::min(a.batch, groups));
-  return launch_pdl(state_update_bulk_kernel<Tin, TPC, DISC, S>, dim3(blocks_x, rb), dim3(kBulkThreads), G::kSmem,
-                    stream, a);
+  if constexpr (BAL) {
+    const long long units = (long long)blocks_x * a.batch;
+    const unsigned grid = unsigned(std::max(1LL, std::min(units, (long long)occupancy * sms)));
+    return launch_pdl(state_update_bulk_kernel<Tin, TPC, DISC, S, BAL>, dim3(grid), dim3(kBulkThreads), G::kSmem,
+                      stream, a);
+  }
+  const int rb = std::max(1, std::min(a.batch, (ctas_per_sm * sms + blocks_x - 1) / blocks_x));
+  return launch_pdl(state_update_bulk_kernel<Tin, TPC, DISC, S, BAL>, dim3(blocks_x, rb), dim3(kBulkThreads),
+                    G::kSmem, stream, a);
 }
 
 // Ring depth and grid, from sweeps on B300 (batch 128, dim 5120, 3-12 stages,
@@ -475,8 +541,8 @@ template <typename Tin, int TPC, int DISC>
 static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + BulkGeom<Tin, TPC, 8>::kCBD - 1) / BulkGeom<Tin, TPC, 8>::kCBD;
-  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4>(a, true, 0, stream);
-  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8>(a, false, 24, stream);
+  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4, true>(a, 0, stream);
+  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8, false>(a, 24, stream);
 }
 
 template <typename Tin, int TPC>
