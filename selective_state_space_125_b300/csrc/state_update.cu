@@ -530,18 +530,19 @@ static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, 
                     G::kSmem, stream, a);
 }
 
-// Ring depth and grid, from sweeps on B300 (batch 128, dim 5120, 3-12 stages,
+// Ring depth and grid, from sweeps on B300 (batch 128, dim 5120, 2-12 stages,
 // 3-32 CTAs per SM):
-// - with few channel blocks (small N), a 4-stage ring and exactly one wave of
-//   CTAs, each walking batch / row-groups rows (N = 16: 18.5 us, against 20.5 us
-//   with 2.7 waves of 4-row CTAs and 22.5 us with 8 stages);
+// - with few channel blocks (small N), exactly one wave of CTAs over balanced
+//   ranges of units and a 3-stage ring (N = 16: 17.15 us, against 17.37 us with
+//   4 stages, 18.0-20.0 us with 5-8 and 22.2 us with 2; on the earlier 2-D
+//   layout one wave beat 2.7 waves of 4-row CTAs, 18.5 against 20.5 us);
 // - with many channel blocks (large N), an 8-stage ring over about 11 rows per
 //   CTA (N = 128: 123 us, against 129 us with 32 rows per CTA).
 template <typename Tin, int TPC, int DISC>
 static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + BulkGeom<Tin, TPC, 8>::kCBD - 1) / BulkGeom<Tin, TPC, 8>::kCBD;
-  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 4, true>(a, 0, stream);
+  if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 3, true>(a, 0, stream);
   return launch_decode_bulk_cfg<Tin, TPC, DISC, 8, false>(a, 24, stream);
 }
 
