@@ -536,14 +536,16 @@ static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, 
 //   ranges of units and a 3-stage ring (N = 16: 17.15 us, against 17.37 us with
 //   4 stages, 18.0-20.0 us with 5-8 and 22.2 us with 2; on the earlier 2-D
 //   layout one wave beat 2.7 waves of 4-row CTAs, 18.5 against 20.5 us);
-// - with many channel blocks (large N), an 8-stage ring over about 11 rows per
-//   CTA (N = 128: 123 us, against 129 us with 32 rows per CTA).
+// - with many channel blocks (large N), a 5-stage ring over about 11 rows per
+//   CTA, 5 CTAs per SM by shared memory (N = 128: 111.8 us, against 112.3 with
+//   6 stages, 112.6 with 4, 127.3 with 8 (3 CTAs per SM) and 157 with 10; 16
+//   or 32 CTAs per SM in place of 24: 115.0 and 112.9 us).
 template <typename Tin, int TPC, int DISC>
 static cudaError_t launch_decode_bulk_disc(const DecodeArgs& a, cudaStream_t stream) {
   const int sms = a.sms > 0 ? a.sms : 148;
   const int blocks_x = (a.dim + BulkGeom<Tin, TPC, 8>::kCBD - 1) / BulkGeom<Tin, TPC, 8>::kCBD;
   if (blocks_x < 2 * sms) return launch_decode_bulk_cfg<Tin, TPC, DISC, 3, true>(a, 0, stream);
-  return launch_decode_bulk_cfg<Tin, TPC, DISC, 8, false>(a, 24, stream);
+  return launch_decode_bulk_cfg<Tin, TPC, DISC, 5, false>(a, 24, stream);
 }
 
 template <typename Tin, int TPC>
