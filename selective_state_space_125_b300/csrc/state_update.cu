@@ -537,7 +537,7 @@ static cudaError_t launch_decode_bulk_cfg(const DecodeArgs& a, int ctas_per_sm, 
 //   4 stages, 18.0-20.0 us with 5-8 and 22.2 us with 2; on the earlier 2-D
 //   layout one wave beat 2.7 waves of 4-row CTAs, 18.5 against 20.5 us);
 // - with many channel blocks (large N), a 5-stage ring over about 11 rows per
-//   CTA, 5 CTAs per SM by shared memory (N = 128: 111.8 us, against 112.3 with
+//   CTA, 4 CTAs per SM (N = 128: 111.8 us, against 112.3 with
 //   6 stages, 112.6 with 4, 127.3 with 8 (3 CTAs per SM) and 157 with 10; 16
 //   or 32 CTAs per SM in place of 24: 115.0 and 112.9 us).
 template <typename Tin, int TPC, int DISC>
