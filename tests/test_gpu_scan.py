@@ -192,6 +192,22 @@ def test_full_size_configs_sampled(dev, name, seed):
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(last))
 
 
+@pytest.mark.parametrize("name", ["m130", "long"])
+def test_full_size_shapes_fp32_sampled(dev, name):
+    """The m130 and long shapes with fp32 inputs (the precise path: expm1f, unscaled state, f32 TMA tiles, the
+    long shape's split-L plan), at 1e-4 on sampled channels the oracle computes one by one."""
+    import dataclasses
+    cfg = dataclasses.replace(SCAN_CONFIGS[name], dtype="f32")
+    inp = make_config_inputs(cfg, seed=5)
+    out, last = run_gpu(inp, dev)
+    rng = np.random.default_rng(321)
+    bs = np.unique(np.concatenate([[0, cfg.batch - 1], rng.integers(0, cfg.batch, 2)]))
+    ds = np.unique(np.concatenate([[0, 1, cfg.dim - 1], rng.integers(0, cfg.dim, 13)]))
+    rout, rlast = sampled_oracle(inp, bs, ds)
+    e1, e2 = parity_err(out[bs][:, :, ds], rout), parity_err(last[bs][:, ds], rlast)
+    assert e1 <= TOL["f32"] and e2 <= TOL["f32"], f"{name} fp32: out {e1:.2e} last {e2:.2e}"
+
+
 # ---- simplified discretisation (Bbar = dt B), against the oracle's variant 1
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("lpc,segments", [(0, 1), (1, 3), (4, 1), (2, 2)])
