@@ -252,13 +252,13 @@ def test_bwd_segments_agree_with_one_segment():
 
 
 # ---- full-size workloads, in the launch configuration bench.py times, on sampled outputs
-def _bwd_full_size(B, D, L, dt_range, seed, chans, dbdc_row):
+def _bwd_full_size(B, D, L, dt_range, seed, chans, dbdc_row, dtype="bf16"):
     import torch
     from selective_state_space_125_b300 import binding
     dev = dev_holder["dev"]
-    inp = make_bwd_inputs(B, D, 16, L, "bf16", seed, dt_range=dt_range)
+    inp = make_bwd_inputs(B, D, 16, L, dtype, seed, dt_range=dt_range)
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev)
-    t = {k: to_torch(inp[k], "bf16", dev) for k in ("u", "delta", "z", "B", "C", "dout")}
+    t = {k: to_torch(inp[k], dtype, dev) for k in ("u", "delta", "z", "B", "C", "dout")}
     g = binding.mamba_selective_scan_bwd(t["u"], t["delta"], f32(inp["A_log"]), t["B"], t["C"], t["dout"],
                                          D=f32(inp["D"]), z=t["z"], delta_bias=f32(inp["delta_bias"]),
                                          initial_state=f32(inp["h0"]), dlast_state=f32(inp["dlast"]))
@@ -287,8 +287,14 @@ def _bwd_full_size(B, D, L, dt_range, seed, chans, dbdc_row):
                                          h0=inp["h0"][r], dlast=inp["dlast"][r])
         errs["dB"] = parity_err(got["dB"][r], full["dB"])
         errs["dC"] = parity_err(got["dC"][r], full["dC"])
-    bad = {k: e for k, e in errs.items() if not e <= TOL["bf16"]}
+    bad = {k: e for k, e in errs.items() if not e <= TOL[dtype]}
     assert not bad, ", ".join(f"{k} {e:.2e}" for k, e in sorted(errs.items()))
+
+
+def test_bwd_full_size_m130_fp32_sampled():
+    """The m130 shape with fp32 inputs (the precise path: expm1f, unscaled state), every per-channel gradient of
+    6 sampled channels and dB/dC of row 0, at 1e-4."""
+    _bwd_full_size(8, 1536, 2048, (1e-3, 1e-1), 4, [0, 31, 32, 777, 1534, 1535], dbdc_row=0, dtype="f32")
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])

@@ -138,6 +138,21 @@ def test_full_size_decode_sampled(dev, name, seed):
     assert parity_err(outs, routs) <= TOL[cfg.dtype], parity_err(outs, routs)
 
 
+@pytest.mark.parametrize("name", ["decode", "decode128"])
+def test_full_size_decode_fp32_sampled(dev, name):
+    """The full decode shapes with fp32 activations (the precise path, f32 bulk tiles), 8 calls, sampled channels
+    followed by the oracle, at 1e-4."""
+    import dataclasses
+    cfg = dataclasses.replace(DECODE_CONFIGS[name], dtype="f32")
+    inp = make_decode_config_inputs(cfg, seed=6)
+    bsel = np.array([0, 77, 127])
+    dsel = np.unique(np.concatenate([[0, cfg.dim - 1], np.random.default_rng(8).integers(0, cfg.dim, 30)]))
+    st, outs = run_decode(inp, dev, 8, bsel=bsel, dsel=dsel)
+    rst, routs = run_decode_oracle(inp, 8, bsel=bsel, dsel=dsel)
+    assert parity_err(st, rst) <= TOL["f32"], parity_err(st, rst)
+    assert parity_err(outs, routs) <= TOL["f32"], parity_err(outs, routs)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("dstate", [16, 128])
 def test_decode_simplified_discretisation(dev, dtype, dstate):
