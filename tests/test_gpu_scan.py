@@ -292,6 +292,29 @@ def test_conv_scan_m130_sampled(dev):
     assert parity_err(last[bs][:, ds], rlast) <= TOL["bf16"]
 
 
+def test_long_sequence_simplified_and_conv_sampled(dev):
+    """The long sequence (split-L plan) with the simplified discretisation, and through the fused conv1d + SiLU,
+    as the benchmark times both: sampled channels against the oracle."""
+    cfg = SCAN_CONFIGS["long"]
+    inp = make_config_inputs(cfg, seed=3)
+    ds = np.array([0, 1, 2047, 2048, 4000, cfg.dim - 1])
+    sub = {k: np.ascontiguousarray(inp[k][:, :, ds]) for k in ("u", "delta", "z")}
+    out, last = run_gpu(inp, dev, plan=dict(lanes_per_channel=0, segments=0, use_tma=0, discretization=1))
+    rout, rlast = oracle.selective_scan(sub["u"], sub["delta"], inp["A_log"][ds], inp["B"], inp["C"], inp["D"][ds],
+                                        sub["z"], inp["delta_bias"][ds], variant=oracle.SIMPLIFIED)
+    assert parity_err(out[:, :, ds], rout) <= TOL["bf16"]
+    assert parity_err(last[:, ds], rlast) <= TOL["bf16"]
+    rng = np.random.default_rng(9)
+    inp["conv_w"] = (rng.standard_normal((cfg.dim, 4)) * 0.5).astype(np.float32)
+    inp["conv_b"] = rng.standard_normal(cfg.dim).astype(np.float32)
+    out, last = run_gpu_conv(inp, dev)
+    u = oracle.causal_conv1d_silu(sub["u"], inp["conv_w"][ds], inp["conv_b"][ds])
+    rout, rlast = oracle.selective_scan(u, sub["delta"], inp["A_log"][ds], inp["B"], inp["C"], inp["D"][ds],
+                                        sub["z"], inp["delta_bias"][ds])
+    assert parity_err(out[:, :, ds], rout) <= TOL["bf16"]
+    assert parity_err(last[:, ds], rlast) <= TOL["bf16"]
+
+
 def test_segmented_scan_under_cuda_graph_capture(dev):
     """A plan with time segments allocates its aggregate workspace with cudaMallocAsync; captured
     in a CUDA graph and replayed, it matches the eager call bit for bit."""
