@@ -138,6 +138,17 @@ def test_full_size_decode_sampled(dev, name, seed):
     assert parity_err(outs, routs) <= TOL[cfg.dtype], parity_err(outs, routs)
 
 
+@pytest.mark.parametrize("dstate", [16, 32])
+def test_decode_unit_ranges_cross_blocks(dev, dstate):
+    """More units (batch rows x channel blocks) than CTA slots, with a ragged last channel block: the bulk kernel's
+    balanced ranges span several rows and cross from one block into the next. Every element against the oracle."""
+    inp = make_decode_inputs(300, 264, dstate, "bf16", seed=40 + dstate, pool=2)
+    st, outs = run_decode(inp, dev, 3)
+    rst, routs = run_decode_oracle(inp, 3)
+    assert parity_err(st, rst) <= TOL["bf16"]
+    assert parity_err(outs, routs) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("name", ["decode", "decode128"])
 def test_full_size_decode_fp32_sampled(dev, name):
     """The full decode shapes with fp32 activations (the precise path, f32 bulk tiles), 8 calls, sampled channels
